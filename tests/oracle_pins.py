@@ -1,0 +1,368 @@
+"""Pins that tie the CPU oracle to what the pages and the mathematics fix.
+
+Every pin is a function ``pin_*(orc) -> None`` that raises ``AssertionError``
+when the oracle build ``orc`` disagrees with something other than itself:
+a brute-force unrolled matrix product, an exact invariant of the delta rule,
+a worked example or number printed on the pages (``tests/golden``), a closed
+form, or a textbook special case.  ``test_oracle.py`` runs them on the faithful
+build, and on builds with a planted mistake to show that each mistake is caught.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _l2(x, eps):
+    return x / np.sqrt((x * x).sum(-1, keepdims=True) + eps)
+
+
+# ---------------------------------------------------------------- brute force
+def brute_force(q, k, v, la, beta, S0, *, g_min=-5.0, l2=True, eps=1e-6):
+    """Unrolled product form of S_t = (I - b k k^T) Diag(a) S_{t-1} + b k v^T.
+
+    S_t = (M_t ... M_1) S0 + sum_s (M_t ... M_{s+1}) b_s k_s v_s^T with dense
+    M_t = (I - b_t k_t k_t^T) Diag(a_t); o_t = S_t^T q_t.  Single head,
+    q, k, la [T, dk], v [T, dv], beta [T], S0 [dk, dv].
+    """
+    T, dk = q.shape
+    if l2:
+        q, k = _l2(q, eps), _l2(k, eps)
+    a = np.exp(np.minimum(np.maximum(la, g_min), 0.0))
+    M = [(np.eye(dk) - beta[t] * np.outer(k[t], k[t])) @ np.diag(a[t]) for t in range(T)]
+    B = [beta[t] * np.outer(k[t], v[t]) for t in range(T)]
+    o, S_t = [], S0
+    for t in range(T):
+        P = np.eye(dk)
+        acc = np.zeros_like(S0)
+        for s in range(t, -1, -1):
+            acc = acc + P @ B[s]
+            P = P @ M[s]
+        S_t = P @ S0 + acc
+        o.append(S_t.T @ q[t])
+    return np.array(o), S_t
+
+
+def _run(orc, q, k, v, la, beta, S0=None, **kw):
+    """Oracle on [T, H, d] fp64 arrays; returns (o [T, H, dv], S_T [N, H, dk, dv]).
+
+    The L2-norm epsilon defaults to 0 here so that unit keys stay exactly unit."""
+    kw.setdefault("eps_l2", 0.0)
+    return orc.prefill(q, k, v, la, beta, S0, **kw)
+
+
+def pin_brute_force(orc):
+    """Oracle == unrolled product on tiny random problems (several shapes,
+    non-unit keys, clamped and unclamped decays, dk != dv)."""
+    for seed, (T, H, dk, dv, l2, eps) in enumerate([(6, 2, 4, 4, True, 1e-6),
+                                                    (8, 1, 5, 7, False, 0.0),
+                                                    (7, 3, 8, 8, True, 0.0),
+                                                    (5, 2, 6, 3, False, 0.0),
+                                                    (4, 1, 3, 5, True, 0.5)]):
+        r = _rng(100 + seed)
+        q = r.normal(size=(T, H, dk))
+        k = r.normal(size=(T, H, dk)) * (0.6 if not l2 else 1.0)
+        v = r.normal(size=(T, H, dv))
+        la = r.uniform(-7.0, 0.2, size=(T, H, dk))
+        beta = r.uniform(0.05, 1.0, size=(T, H))
+        S0 = r.normal(size=(1, H, dk, dv))
+        o, S_T = _run(orc, q, k, v, la, beta, S0, l2norm_qk=l2, eps_l2=eps)
+        for h in range(H):
+            o_ref, S_ref = brute_force(q[:, h], k[:, h], v[:, h], la[:, h], beta[:, h],
+                                       S0[0, h], l2=l2, eps=eps)
+            np.testing.assert_allclose(o[:, h], o_ref, rtol=1e-11, atol=1e-11)
+            np.testing.assert_allclose(S_T[0, h], S_ref, rtol=1e-11, atol=1e-11)
+
+
+# ---------------------------------------------------------------- delta rule
+def pin_overwrite(orc):
+    """beta = 1 and a unit key replace whatever was stored along k with v
+    exactly (the delta rule as one gradient step on 1/2 |S^T k - v|^2), and
+    leave every direction orthogonal to k with the faded state."""
+    r = _rng(7)
+    d = 8
+    T = 5
+    k = _unit(r.normal(size=(T, 1, d)))
+    q = k.copy()                       # read back along the key just written
+    v = r.normal(size=(T, 1, d))
+    la = r.uniform(-3.0, 0.0, size=(T, 1, d))
+    beta = np.ones((T, 1))
+    S0 = r.normal(size=(1, 1, d, d))
+    o, _ = _run(orc, q, k, v, la, beta, S0)
+    np.testing.assert_allclose(o[:, 0], v[:, 0], rtol=0, atol=1e-12)
+    # one step, check the orthogonal complement keeps Diag(a) S0
+    o1, S1 = _run(orc, q[:1], k[:1], v[:1], la[:1], beta[:1], S0)
+    faded = np.exp(la[0, 0])[:, None] * S0[0, 0]
+    x = r.normal(size=d)
+    x = x - (x @ k[0, 0]) * k[0, 0]     # x orthogonal to k
+    np.testing.assert_allclose(S1[0, 0].T @ x, faded.T @ x, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(S1[0, 0].T @ k[0, 0], v[0, 0], rtol=0, atol=1e-12)
+
+
+def pin_meeting(orc):
+    """The pages' whiteboard example, built exactly: orthonormal rows, alpha = 1,
+    beta = 1.  Editing the meeting-day row changes only that row; the board
+    keeps three rows."""
+    g = golden("meeting.json")
+    d = 4
+    keys, vals = g["key_rows"], g["value_codes"]
+    writes = g["writes"]
+    T = len(writes)
+    k = np.zeros((T, 1, d))
+    v = np.zeros((T, 1, d))
+    for t, (row, val) in enumerate(writes):
+        k[t, 0, keys[row]] = 1.0
+        v[t, 0, vals[val]] = 1.0
+    q = k.copy()
+    la = np.zeros((T, 1, d))
+    beta = np.ones((T, 1))
+    _, S_before = _run(orc, q[:3], k[:3], v[:3], la[:3], beta[:3])
+    _, S_after = _run(orc, q, k, v, la, beta)
+    B0, B1 = S_before[0, 0], S_after[0, 0]
+    for row, val in g["expected_board"].items():
+        e = np.zeros(d)
+        e[vals[val]] = 1.0
+        np.testing.assert_array_equal(B1[keys[row]], e)
+    for row in ("client", "budget"):           # untouched rows: bit-exact
+        np.testing.assert_array_equal(B1[keys[row]], B0[keys[row]])
+    assert int((np.abs(B1).sum(1) > 0).sum()) == g["expected_rows"]
+
+
+# ------------------------------------------------- linear-attention reductions
+def pin_linear_attention(orc):
+    """alpha = 1 reductions (see the linear-attention paragraph of the pages):
+    L0 alpha=1, beta=0: S never changes, o_t = S0^T q_t exactly;
+    L1 alpha=1, orthonormal keys, S0=0: o_t = sum_{s<=t} beta_s (q_t.k_s) v_s,
+       and with beta = 1 that is plain (unnormalised) linear attention;
+    L2 alpha=1, S0=0, generic keys, beta = eps -> 0: o_t/eps -> sum (q_t.k_s) v_s."""
+    r = _rng(11)
+    T, d = 6, 8
+    q = _unit(r.normal(size=(T, 1, d)))
+    k = _unit(r.normal(size=(T, 1, d)))
+    v = r.normal(size=(T, 1, d))
+    la = np.zeros((T, 1, d))
+    S0 = r.normal(size=(1, 1, d, d))
+    # L0
+    o, S_T = _run(orc, q, k, v, la, np.zeros((T, 1)), S0)
+    np.testing.assert_array_equal(S_T[0, 0], S0[0, 0])
+    np.testing.assert_allclose(o[:, 0], q[:, 0] @ S0[0, 0], rtol=0, atol=1e-13)
+    # L1 (orthonormal keys: columns of a random orthogonal matrix)
+    Qm, _ = np.linalg.qr(r.normal(size=(d, d)))
+    ko = Qm.T[:T].reshape(T, 1, d)
+    for beta in (r.uniform(0.1, 1.0, size=(T, 1)), np.ones((T, 1))):
+        o, _ = _run(orc, q, ko, v, la, beta)
+        ref = np.array([sum(beta[s, 0] * (q[t, 0] @ ko[s, 0]) * v[s, 0] for s in range(t + 1))
+                        for t in range(T)])
+        np.testing.assert_allclose(o[:, 0], ref, rtol=0, atol=1e-12)
+    # L2
+    eps = 1e-7
+    o, _ = _run(orc, q, k, v, la, np.full((T, 1), eps))
+    ref = np.array([sum((q[t, 0] @ k[s, 0]) * v[s, 0] for s in range(t + 1)) for t in range(T)])
+    np.testing.assert_allclose(o[:, 0] / eps, ref, rtol=0, atol=1e-5)
+
+
+# ---------------------------------------------------------------- decay
+def pin_half_life(orc):
+    """With beta = 0 and S0 = I a channel of constant alpha decays as alpha^n;
+    alpha = 0.99 halves it at n = ln 0.5 / ln 0.99 = 68.97, i.e. about 69
+    tokens; log alpha = ln 0.5 / n gives exactly one half after n tokens."""
+    g = golden("half_life.json")
+    alpha = g["alpha"]
+    n_half = math.log(0.5) / math.log(alpha)
+    assert round(n_half) == g["n_half_about"]
+    d, T = 4, 80
+    q = np.tile(np.eye(d)[None, None, 0], (T, 1, 1))    # read channel 0
+    k = np.tile(np.eye(d)[None, None, 1], (T, 1, 1))
+    v = np.zeros((T, 1, d))
+    la = np.full((T, 1, d), math.log(alpha))
+    S0 = np.eye(d)[None, None]
+    o, _ = _run(orc, q, k, v, la, np.zeros((T, 1)), S0, l2norm_qk=False)
+    trace = o[:, 0, 0]                                   # alpha^(t+1)
+    np.testing.assert_allclose(trace, alpha ** np.arange(1, T + 1), rtol=1e-13)
+    first_below = int(np.argmax(trace <= 0.5)) + 1
+    assert first_below == g["n_half_about"]
+    n = 50
+    la2 = np.full((n, 1, d), math.log(0.5) / n)
+    o2, _ = _run(orc, q[:n], k[:n], v[:n], la2, np.zeros((n, 1)), S0, l2norm_qk=False)
+    assert abs(o2[-1, 0, 0] - 0.5) < 1e-13
+
+
+def pin_floor(orc):
+    """log alpha is floored at -5 (retention >= e^-5 ~ 0.0067) and capped at 0."""
+    g = golden("floor.json")
+    d = 4
+    q = np.eye(d)[None, None, 0]
+    k = np.eye(d)[None, None, 1]
+    v = np.zeros((1, 1, d))
+    S0 = np.eye(d)[None, None]
+    o7, _ = _run(orc, q, k, v, np.full((1, 1, d), -7.0), np.zeros((1, 1)), S0, l2norm_qk=False)
+    o5, _ = _run(orc, q, k, v, np.full((1, 1, d), g["log_alpha_floor"]), np.zeros((1, 1)), S0,
+                 l2norm_qk=False)
+    np.testing.assert_array_equal(o7, o5)
+    assert round(float(o5[0, 0, 0]), g["decimals"]) == g["retention_floor_about"]
+    op, _ = _run(orc, q, k, v, np.full((1, 1, d), 0.5), np.zeros((1, 1)), S0, l2norm_qk=False)
+    assert op[0, 0, 0] == 1.0
+    # the floor also holds inside a full update
+    r = _rng(5)
+    T = 6
+    qq, kk, vv = r.normal(size=(T, 1, d)), r.normal(size=(T, 1, d)), r.normal(size=(T, 1, d))
+    bb = r.uniform(0.2, 0.9, size=(T, 1))
+    lo = r.uniform(-12.0, -5.0, size=(T, 1, d))
+    a1, s1 = _run(orc, qq, kk, vv, lo, bb)
+    a2, s2 = _run(orc, qq, kk, vv, np.full_like(lo, -5.0), bb)
+    np.testing.assert_array_equal(a1, a2)
+    np.testing.assert_array_equal(s1, s2)
+
+
+def pin_scalar_decay(orc):
+    """All channels equal reduces KDA to Gated DeltaNet (one decay per head):
+    S_t = a_t (I - b k k^T) S_{t-1} + b k v^T, here as a separate scalar loop."""
+    r = _rng(13)
+    T, d = 9, 6
+    q, k = _unit(r.normal(size=(T, d))), _unit(r.normal(size=(T, d)))
+    v = r.normal(size=(T, d))
+    a = r.uniform(0.3, 1.0, size=T)
+    b = r.uniform(0.1, 1.0, size=T)
+    S = r.normal(size=(d, d))
+    S0 = S.copy()
+    ref = []
+    for t in range(T):
+        S = a[t] * (S - b[t] * np.outer(k[t], k[t] @ S)) + b[t] * np.outer(k[t], v[t])
+        ref.append(S.T @ q[t])
+    la = np.repeat(np.log(a)[:, None, None], d, axis=2)
+    o, S_T = _run(orc, q[:, None], k[:, None], v[:, None], la, b[:, None], S0[None, None])
+    np.testing.assert_allclose(o[:, 0], np.array(ref), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S_T[0, 0], S, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- prologue
+def pin_l2norm(orc):
+    """With L2 normalisation on, rescaling q or k by a positive factor changes
+    nothing (the layer normalises them; same section as the recurrence)."""
+    r = _rng(17)
+    T, H, d = 7, 2, 8
+    q, k, v = r.normal(size=(T, H, d)), r.normal(size=(T, H, d)), r.normal(size=(T, H, d))
+    la = r.uniform(-5, 0, size=(T, H, d))
+    b = r.uniform(0.1, 1, size=(T, H))
+    o1, s1 = _run(orc, q, k, v, la, b, eps_l2=0.0)
+    o2, s2 = _run(orc, 7.0 * q, 3.0 * k, v, la, b, eps_l2=0.0)
+    np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(s1, s2, rtol=1e-12, atol=1e-12)
+    qn = q / np.linalg.norm(q, axis=-1, keepdims=True)
+    kn = k / np.linalg.norm(k, axis=-1, keepdims=True)
+    o3, _ = _run(orc, qn, kn, v, la, b, l2norm_qk=False)
+    np.testing.assert_allclose(o1, o3, rtol=1e-12, atol=1e-12)
+
+
+def pin_beta_logit(orc):
+    """beta given as a logit equals beta given as sigmoid(logit)."""
+    r = _rng(19)
+    T, H, d = 6, 2, 8
+    q, k, v = r.normal(size=(T, H, d)), r.normal(size=(T, H, d)), r.normal(size=(T, H, d))
+    la = r.uniform(-5, 0, size=(T, H, d))
+    z = r.normal(size=(T, H))
+    o1, _ = _run(orc, q, k, v, la, z, beta_is_logit=True)
+    o2, _ = _run(orc, q, k, v, la, 1.0 / (1.0 + np.exp(-z)))
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- structure
+def pin_split_and_decode(orc):
+    """Prefix caching: prefill(T) = prefill(T1) then prefill(rest) from S_T1,
+    and = T single-token decode steps; packed sequences = separate calls;
+    a zero-length sequence returns its S0."""
+    r = _rng(23)
+    T, H, d = 11, 2, 6
+    q, k, v = r.normal(size=(T, H, d)), r.normal(size=(T, H, d)), r.normal(size=(T, H, d))
+    la = r.uniform(-5, 0, size=(T, H, d))
+    b = r.uniform(0.1, 1, size=(T, H))
+    S0 = r.normal(size=(1, H, d, d))
+    o, S_T = _run(orc, q, k, v, la, b, S0)
+    T1 = 4
+    oa, Sa = _run(orc, q[:T1], k[:T1], v[:T1], la[:T1], b[:T1], S0)
+    ob, Sb = _run(orc, q[T1:], k[T1:], v[T1:], la[T1:], b[T1:], Sa)
+    np.testing.assert_allclose(np.concatenate([oa, ob]), o, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(Sb, S_T, rtol=1e-13, atol=1e-13)
+    S = S0.copy()
+    for t in range(T):
+        ot, S = orc.decode_step(q[t:t + 1], k[t:t + 1], v[t:t + 1], la[t:t + 1], b[t:t + 1], S,
+                                eps_l2=0.0)
+        np.testing.assert_allclose(ot[0], o[t], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(S, S_T, rtol=1e-13, atol=1e-13)
+    # packed: [T1 tokens | 0 tokens | rest]
+    cu = np.array([0, T1, T1, T], dtype=np.int32)
+    S03 = r.normal(size=(3, H, d, d))
+    op, Sp = orc.prefill(q, k, v, la, b, S03, cu, eps_l2=0.0)
+    o1, S1 = _run(orc, q[:T1], k[:T1], v[:T1], la[:T1], b[:T1], S03[0:1])
+    o3, S3 = _run(orc, q[T1:], k[T1:], v[T1:], la[T1:], b[T1:], S03[2:3])
+    np.testing.assert_allclose(op, np.concatenate([o1, o3]), rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(Sp[0], S1[0], rtol=1e-13, atol=1e-13)
+    np.testing.assert_array_equal(Sp[1], S03[1])
+    np.testing.assert_allclose(Sp[2], S3[0], rtol=1e-13, atol=1e-13)
+    # head subset = the same heads of the full run
+    o_h, S_h = _run(orc, q, k, v, la, b, S0, heads=(1, 1))
+    np.testing.assert_array_equal(o_h[:, 0], o[:, 1])
+    np.testing.assert_array_equal(S_h[0, 0], S_T[0, 1])
+
+
+def pin_gated_rmsnorm(orc):
+    """Closed forms of the per-head RMSNorm x sigmoid gate: a constant vector
+    c*1 maps to sign(c)*sigmoid(g); a one-hot a*e_j maps to sqrt(dv)*sigmoid(g)
+    at j; a weight vector scales channel-wise."""
+    dv = 16
+    o = np.zeros((3, 2, dv))
+    o[0, 0] = 2.5
+    o[0, 1] = -0.75
+    o[1, 0, 5] = 3.0
+    o[1, 1, 0] = -0.1
+    o[2] = _rng(29).normal(size=(2, dv))
+    gate = _rng(31).normal(size=(3, 2, dv))
+    sg = 1.0 / (1.0 + np.exp(-gate))
+    y = orc.gated_rmsnorm(o, gate, eps=0.0)
+    np.testing.assert_allclose(y[0, 0], sg[0, 0], rtol=1e-14)
+    np.testing.assert_allclose(y[0, 1], -sg[0, 1], rtol=1e-14)
+    assert abs(y[1, 0, 5] - math.sqrt(dv) * sg[1, 0, 5]) < 1e-13
+    assert np.count_nonzero(y[1, 0]) == 1
+    assert abs(y[1, 1, 0] + math.sqrt(dv) * sg[1, 1, 0]) < 1e-13
+    # rms of the normalised vector is 1 before the gate
+    yn = orc.gated_rmsnorm(o[2:3], np.full((1, 2, dv), 50.0), eps=0.0)
+    np.testing.assert_allclose(np.sqrt((yn ** 2).mean(-1)), 1.0, rtol=1e-12)
+    w = np.linspace(0.5, 2.0, dv)
+    yw = orc.gated_rmsnorm(o, gate, w=w, eps=0.0)
+    np.testing.assert_allclose(yw, y * w, rtol=1e-14)
+    # head offset selects the gate's heads
+    y1 = orc.gated_rmsnorm(o[:, 1:2], gate, eps=0.0, h0=1)
+    np.testing.assert_allclose(y1[:, 0], y[:, 1], rtol=1e-14)
+
+
+ALL_PINS = [
+    pin_brute_force,
+    pin_overwrite,
+    pin_meeting,
+    pin_linear_attention,
+    pin_half_life,
+    pin_floor,
+    pin_scalar_decay,
+    pin_l2norm,
+    pin_beta_logit,
+    pin_split_and_decode,
+    pin_gated_rmsnorm,
+]

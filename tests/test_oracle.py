@@ -1,0 +1,66 @@
+"""The CPU oracle against its pins (CPU only).
+
+``oracle_pins`` holds checks that tie the oracle to the pages and to the
+mathematics.  The faithful build must pass every pin; each build with a planted
+mistake (a dropped fade, a read before the write, a wrong sign, a wrong index,
+a dropped beta, a missing floor, the fade in the wrong place, a missing key
+normalisation, the wrong probe vector) must fail at least one of them.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle import build as oracle_build
+from tests import oracle_pins
+
+MUTATIONS = {
+    1: "no fade",
+    2: "read before write",
+    3: "erase with the wrong sign",
+    4: "wrong state row in the read",
+    5: "beta dropped from the write",
+    6: "no floor on log alpha",
+    7: "fade after the write",
+    8: "key not normalised",
+    9: "state probed with the query",
+}
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    assert orc.mutation == 0
+    pin(orc)
+
+
+@pytest.mark.parametrize("m", sorted(MUTATIONS), ids=lambda m: MUTATIONS[m].replace(" ", "_"))
+def test_pins_catch_planted_mistake(tmp_path, m):
+    path = oracle_build.build(out_path=os.path.join(tmp_path, f"m{m}.so"), mutation=m)
+    bad = oracle.Oracle(path)
+    assert bad.mutation == m
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(bad)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught planted mistake {m} ({MUTATIONS[m]})"
+
+
+def test_state_sizes_golden():
+    """The state layout [N, H, d_k, d_v] fp32 holds the pages' counts."""
+    import numpy as np
+    g = oracle_pins.golden("state_sizes.json")
+    per_layer = int(np.prod((1, g["heads"], g["d_k"], g["d_v"])))
+    assert per_layer == g["numbers_per_layer"]
+    assert per_layer * g["kda_layers"] == g["numbers_per_sequence"]
+    assert round(g["numbers_per_sequence"] * 4 / 2 ** 20) == g["mib_fp32"]
+
+
+def test_oracle_rejects_bad_arguments(orc):
+    import numpy as np
+    q = np.zeros((4, 1, 4))
+    with pytest.raises(ValueError):
+        orc.prefill(q, q, q, q, np.zeros((4, 1)), None, np.array([0, 3, 2], dtype=np.int32))
+    with pytest.raises(ValueError):
+        orc.prefill(q, q, q, q, np.zeros((4, 1)), None, None, heads=(0, 2))
