@@ -1,0 +1,253 @@
+"""Thin ctypes binding of libkda.so (the C ABI in ``include/kda.h``).
+
+The functions carry the C entry points' names and do argument marshalling
+only: shapes are read off the tensors, outputs and the workspace are
+allocated with PyTorch when the caller does not pass them, and the call goes
+to the library on the current CUDA stream.  Every step of the computation runs
+in the library's CUDA kernels; there is no Python or CPU fallback, and a
+missing or unloadable library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+KDA_OK = 0
+KDA_ERR_ARG = -1
+KDA_ERR_SHAPE = -2
+KDA_ERR_DTYPE = -3
+KDA_ERR_ALIGN = -4
+KDA_ERR_UNSUPPORTED = -5
+KDA_ERR_CUDA = -6
+KDA_ERR_TIMEOUT = -7
+KDA_ERR_WORKSPACE = -8
+
+KDA_F32 = 0
+KDA_BF16 = 1
+
+IMPLS = {"auto": 0, "simt": 1, "tc": 2}
+
+
+class kda_options(ctypes.Structure):
+    """Mirror of ``struct kda_options`` (field order and types as in kda.h)."""
+    _fields_ = [
+        ("chunk", ctypes.c_int),
+        ("l2norm_qk", ctypes.c_int),
+        ("beta_is_logit", ctypes.c_int),
+        ("g_min", ctypes.c_float),
+        ("q_scale", ctypes.c_float),
+        ("eps_l2", ctypes.c_float),
+        ("eps_norm", ctypes.c_float),
+        ("gate", ctypes.c_void_p),
+        ("norm_weight", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("max_seqlen", ctypes.c_int),
+        ("impl", ctypes.c_int),
+        ("debug_timeout", ctypes.c_int),
+        ("timeout_spins", ctypes.c_longlong),
+    ]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {kda_status_string(status)} ({status})")
+
+
+_LIB = None
+EXPORTS = ("kda_options_init", "kda_prefill", "kda_prefill_workspace_size", "kda_decode_step",
+           "kda_gated_rmsnorm", "kda_get_last_error", "kda_status_string", "kda_abi_version")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libkda.so (building it first if it is missing or stale)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    if path is None:
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    po = ctypes.POINTER(kda_options)
+    lib.kda_options_init.argtypes = [po]
+    lib.kda_options_init.restype = None
+    lib.kda_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, vp, vp, ci, ci, ci, ci, ci, po, vp]
+    lib.kda_prefill.restype = ci
+    lib.kda_prefill_workspace_size.argtypes = [ci, ci, ci, ci, ci, po]
+    lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, po, vp]
+    lib.kda_decode_step.restype = ci
+    lib.kda_gated_rmsnorm.argtypes = [vp, vp, vp, vp, ci, ci, ci, cf, ci, vp]
+    lib.kda_gated_rmsnorm.restype = ci
+    lib.kda_get_last_error.argtypes = [vp]
+    lib.kda_get_last_error.restype = ci
+    lib.kda_status_string.argtypes = [ci]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_abi_version.restype = ci
+    if path == _build.LIB or _LIB is None:
+        _LIB = lib
+    return lib
+
+
+def kda_status_string(status: int) -> str:
+    return load().kda_status_string(int(status)).decode()
+
+
+def kda_abi_version() -> int:
+    return load().kda_abi_version()
+
+
+def kda_options_init(**overrides) -> kda_options:
+    """Default options (C kda_options_init), then keyword overrides."""
+    opt = kda_options()
+    load().kda_options_init(ctypes.byref(opt))
+    for key, val in overrides.items():
+        if key == "impl" and isinstance(val, str):
+            val = IMPLS[val]
+        setattr(opt, key, val)
+    return opt
+
+
+# ---------------------------------------------------------------- marshalling
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _stream(stream) -> int | None:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("libkda takes CUDA tensors (device memory)")
+        if not t.is_contiguous():
+            raise ValueError("libkda takes contiguous tensors")
+
+
+def _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+          eps_norm, workspace, workspace_bytes, max_seqlen, impl, debug_timeout,
+          timeout_spins) -> kda_options:
+    return kda_options_init(
+        chunk=int(chunk), l2norm_qk=int(bool(l2norm_qk)), beta_is_logit=int(bool(beta_is_logit)),
+        g_min=float(g_min), q_scale=float(q_scale), eps_l2=float(eps_l2),
+        eps_norm=float(eps_norm), gate=_ptr(gate), norm_weight=_ptr(norm_weight),
+        workspace=_ptr(workspace), workspace_bytes=int(workspace_bytes),
+        max_seqlen=int(max_seqlen), impl=impl, debug_timeout=int(bool(debug_timeout)),
+        timeout_spins=int(timeout_spins))
+
+
+def kda_prefill_workspace_size(T_total: int, N: int, H: int, d_k: int, d_v: int,
+                               opt: kda_options | None = None) -> int:
+    o = opt if opt is not None else kda_options_init()
+    return int(load().kda_prefill_workspace_size(T_total, N, H, d_k, d_v, ctypes.byref(o)))
+
+
+def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | None = None,
+                o=None, S_T=None, *, gate=None, norm_weight=None, chunk: int = 0,
+                l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
+                q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
+                workspace=None, max_seqlen: int = 0, impl="auto", debug_timeout: bool = False,
+                timeout_spins: int = 0, stream=None):
+    """Chunked prefill (C ``kda_prefill``).
+
+    q, k, log_alpha [T, H, d_k]; v [T, H, d_v]; beta [T, H]; S0 [N, H, d_k, d_v]
+    fp32 or None; cu_seqlens [N+1] int32 (device) or None.  Returns (o, S_T);
+    o holds y = RMSNorm(o) * w * sigmoid(gate) when ``gate`` is given.
+    """
+    import torch
+    _check_cuda(q, k, v, log_alpha, beta, S0, cu_seqlens, gate, norm_weight, o, S_T)
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+    N = N or 1
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
+    if S_T is None:
+        S_T = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    impl_code = IMPLS[impl] if isinstance(impl, str) else int(impl)
+    opt = _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+                eps_norm, None, 0, max_seqlen, impl_code, debug_timeout, timeout_spins)
+    need = kda_prefill_workspace_size(T, N, H, d_k, d_v, opt)
+    if need > 0:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        opt.workspace = _ptr(workspace)
+        opt.workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(S0),
+                            _ptr(cu_seqlens), N, _ptr(o), _ptr(S_T), T, H, d_k, d_v, dt,
+                            ctypes.byref(opt), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill")
+    return o, S_T
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weight=None,
+                    l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
+                    q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
+                    stream=None):
+    """One decode step (C ``kda_decode_step``); S [N, H, d_k, d_v] is updated in place.
+    Returns o [N, H, d_v]."""
+    import torch
+    _check_cuda(q, k, v, log_alpha, beta, S, o, gate, norm_weight)
+    N, H, d_k = q.shape
+    d_v = v.shape[2]
+    if o is None:
+        o = torch.empty((N, H, d_v), dtype=q.dtype, device=q.device)
+    opt = _opts(gate, norm_weight, 0, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+                eps_norm, None, 0, 0, 0, False, 0)
+    rc = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                _ptr(S), _ptr(o), N, H, d_k, d_v, _dtype_code(q),
+                                ctypes.byref(opt), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+    return o
+
+
+def kda_gated_rmsnorm(o, gate, w=None, y=None, *, eps: float = 1e-6, stream=None):
+    """y = o / sqrt(mean(o^2) + eps) * w * sigmoid(gate) per (row, head)
+    (C ``kda_gated_rmsnorm``); o, gate [rows, H, d_v]."""
+    import torch
+    _check_cuda(o, gate, w, y)
+    rows, H, d_v = o.shape
+    if y is None:
+        y = torch.empty_like(o)
+    rc = load().kda_gated_rmsnorm(_ptr(o), _ptr(gate), _ptr(w), _ptr(y), rows, H, d_v,
+                                  float(eps), _dtype_code(o), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_gated_rmsnorm")
+    return y
+
+
+def kda_get_last_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    return int(load().kda_get_last_error(_stream(stream)))

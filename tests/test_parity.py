@@ -1,0 +1,252 @@
+"""GPU parity: libkda.so (through its C ABI) against the fp64 CPU oracle.
+
+Both sides get the same seeded inputs (``inputs``).  Small cases are compared
+element by element over whole tensors; the full-size workloads are compared on
+sampled heads / sequences, which the oracle computes one by one.  Tolerances:
+max-abs <= 2e-2 and rel-L2 <= 5e-3 for bf16 operands, 1e-4 for the fp32 path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_recurrence_prefill_gb300 import inputs, kda
+from tests.parity_util import TOL_BF16, TOL_F32, assert_close
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = ["simt"]
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda")
+
+
+def _oracle_prefill(inp, heads=None, gate=True):
+    """Oracle o (or y) and S_T for the given head indices (all by default)."""
+    idx = list(range(inp.H)) if heads is None else list(heads)
+    sl = lambda t: t[:, idx].cpu() if t is not None else None  # noqa: E731
+    S0 = inp.S0[:, idx].cpu() if inp.S0 is not None else None
+    cu = inp.cu_seqlens.cpu() if inp.cu_seqlens is not None else None
+    o, S_T = oracle.prefill(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.log_alpha), sl(inp.beta),
+                            S0, cu, N=inp.N)
+    if gate and inp.gate is not None:
+        o = oracle.gated_rmsnorm(o, sl(inp.gate))
+    return o, S_T, idx
+
+
+def _gpu_prefill(inp, impl, gate=True, **kw):
+    o, S_T = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0,
+                             inp.cu_seqlens, N=inp.N, gate=inp.gate if gate else None,
+                             impl=impl, **kw)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_error() == kda.KDA_OK
+    return o, S_T
+
+
+def _check(inp, impl, tol, heads=None, gate=True, **kw):
+    o, S_T = _gpu_prefill(inp, impl, gate=gate, **kw)
+    o_ref, S_ref, idx = _oracle_prefill(inp, heads, gate=gate)
+    assert_close(o[:, idx], o_ref, tol, f"{inp.name} o/y")
+    assert_close(S_T[:, idx], S_ref, tol, f"{inp.name} S_T")
+    return o, S_T
+
+
+# --------------------------------------------------------------------- small
+def test_tiny_fp32():
+    """Tiny workload: H=2, T=128, d=32, fp32, chunk 16 (whole tensors)."""
+    dev = _cuda()
+    inp = inputs.tiny(dev)
+    _check(inp, "simt", TOL_F32)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("T", [1, 15, 64, 200, 1000])
+def test_k3_shaped_small(impl, T):
+    """K3-shaped distributions, 4 heads, ragged lengths, gated output."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=4, T=T, seed=11 + T)
+    _check(inp, impl, TOL_BF16)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_fp32_path_head_sizes(d):
+    dev = _cuda()
+    inp = inputs.k3(dev, H=3, T=100, d=d, dtype=torch.float32, seed=5)
+    _check(inp, "simt", TOL_F32)
+
+
+def test_varlen_small_edges():
+    """Packed sequences with empty, single-token and ragged members."""
+    dev = _cuda()
+    lens = [0, 1, 17, 64, 65, 0, 130, 3]
+    inp = inputs.varlen(dev, H=3, lengths=lens)
+    inp.S0 = torch.randn((len(lens), 3, 128, 128), device=dev) * 0.05
+    for impl in IMPLS:
+        o, S_T = _check(inp, impl, TOL_BF16)
+        # empty sequences hand back their initial state
+        torch.testing.assert_close(S_T[0], inp.S0[0], rtol=0, atol=0)
+        torch.testing.assert_close(S_T[5], inp.S0[5], rtol=0, atol=0)
+
+
+def test_no_tokens():
+    dev = _cuda()
+    S0 = torch.randn((2, 3, 64, 64), device=dev)
+    S_T = torch.empty_like(S0)
+    cu = torch.zeros(3, dtype=torch.int32, device=dev)
+    lib = kda.load()
+    import ctypes
+    opt = kda.kda_options_init()
+    rc = lib.kda_prefill(None, None, None, None, None, S0.data_ptr(), cu.data_ptr(), 2, None,
+                         S_T.data_ptr(), 0, 3, 64, 64, kda.KDA_BF16, ctypes.byref(opt),
+                         torch.cuda.current_stream().cuda_stream)
+    assert rc == kda.KDA_OK
+    torch.cuda.synchronize()
+    torch.testing.assert_close(S_T, S0, rtol=0, atol=0)
+
+
+def test_options_logit_beta_qscale_weight():
+    """beta as logit, q_scale and an RMSNorm weight, against the oracle."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=2, T=77, seed=3)
+    z = torch.randn((inp.T, inp.H), device=dev).to(torch.bfloat16)
+    w = torch.linspace(0.5, 1.5, 128, device=dev)
+    for impl in IMPLS:
+        o, S_T = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, z, inp.S0, gate=inp.gate,
+                                 norm_weight=w, beta_is_logit=True, q_scale=0.5, impl=impl)
+        torch.cuda.synchronize()
+        o_ref, S_ref = oracle.prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(),
+                                      inp.log_alpha.cpu(), z.cpu(), inp.S0.cpu(),
+                                      beta_is_logit=True, q_scale=0.5)
+        y_ref = oracle.gated_rmsnorm(o_ref, inp.gate.cpu(), w=w.cpu())
+        assert_close(o, y_ref, TOL_BF16, "y")
+        assert_close(S_T, S_ref, TOL_BF16, "S_T")
+
+
+def test_split_equals_whole():
+    """Prefix caching: prefill(T) == prefill(T1) then prefill(T - T1) from S_T1."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=2, T=300, seed=4)
+    for impl in IMPLS:
+        o, S_T = _gpu_prefill(inp, impl)
+        T1 = 100
+        sl = lambda t, a, b: t[a:b].contiguous()  # noqa: E731
+        o1, S1 = kda.kda_prefill(sl(inp.q, 0, T1), sl(inp.k, 0, T1), sl(inp.v, 0, T1),
+                                 sl(inp.log_alpha, 0, T1), sl(inp.beta, 0, T1), inp.S0,
+                                 gate=sl(inp.gate, 0, T1), impl=impl)
+        o2, S2 = kda.kda_prefill(sl(inp.q, T1, None), sl(inp.k, T1, None), sl(inp.v, T1, None),
+                                 sl(inp.log_alpha, T1, None), sl(inp.beta, T1, None), S1,
+                                 gate=sl(inp.gate, T1, None), impl=impl)
+        torch.cuda.synchronize()
+        assert_close(torch.cat([o1, o2]), o.float(), TOL_BF16, "split o")
+        assert_close(S2, S_T, TOL_BF16, "split S_T")
+
+
+def test_gated_rmsnorm_standalone():
+    dev = _cuda()
+    for dt, tol in ((torch.bfloat16, TOL_BF16), (torch.float32, TOL_F32)):
+        o = (torch.randn((50, 3, 128), device=dev) * 0.3).to(dt)
+        g = torch.randn((50, 3, 128), device=dev).to(dt)
+        w = torch.rand(128, device=dev) + 0.5
+        y = kda.kda_gated_rmsnorm(o, g, w)
+        torch.cuda.synchronize()
+        ref = oracle.gated_rmsnorm(o.cpu().double().numpy(), g.cpu(), w=w.cpu())
+        assert_close(y, ref, tol, "rmsnorm")
+        y2 = kda.kda_gated_rmsnorm(o, g, w, y=o)       # in place
+        torch.cuda.synchronize()
+        assert_close(y2, ref, tol, "rmsnorm in place")
+
+
+# --------------------------------------------------------------------- decode
+def _decode_run(d, steps, N=4, H=3, dtype=torch.bfloat16, gate=False):
+    dev = _cuda()
+    di = inputs.decode(dev, N=N, H=H, d=d, steps=steps, dtype=dtype)
+    S = di.S.clone()
+    S_ref = di.S.cpu().double().numpy()
+    for t in range(steps):
+        g = torch.randn((N, H, d), device=dev).to(dtype) if gate else None
+        o = kda.kda_decode_step(di.q[t], di.k[t], di.v[t], di.log_alpha[t], di.beta[t], S, gate=g)
+        o_ref, S_ref = oracle.decode_step(di.q[t].cpu(), di.k[t].cpu(), di.v[t].cpu(),
+                                          di.log_alpha[t].cpu(), di.beta[t].cpu(), S_ref)
+        if g is not None:
+            o_ref = oracle.gated_rmsnorm(o_ref, g.cpu())
+        torch.cuda.synchronize()
+        tol = TOL_BF16 if dtype == torch.bfloat16 else TOL_F32
+        assert_close(o, o_ref, tol, f"decode o step {t}")
+    assert_close(S, S_ref, TOL_BF16 if dtype == torch.bfloat16 else TOL_F32, "decode S")
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_decode_small(d):
+    _decode_run(d, steps=5)
+
+
+def test_decode_fp32_and_gate():
+    _decode_run(64, steps=3, dtype=torch.float32)
+    _decode_run(128, steps=3, gate=True)
+
+
+def test_prefill_equals_decode_steps():
+    """T decode steps reach the state one prefill of T tokens reaches."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=2, T=40, seed=8)
+    S = inp.S0.clone()
+    outs = []
+    for t in range(inp.T):
+        outs.append(kda.kda_decode_step(inp.q[t:t + 1], inp.k[t:t + 1], inp.v[t:t + 1],
+                                        inp.log_alpha[t:t + 1], inp.beta[t:t + 1], S))
+    for impl in IMPLS:
+        o, S_T = _gpu_prefill(inp, impl, gate=False)
+        assert_close(torch.cat(outs).float(), o.float(), TOL_BF16, "decode vs prefill o")
+        assert_close(S, S_T, TOL_BF16, "decode vs prefill S")
+
+
+# ------------------------------------------------------------ full workloads
+@pytest.mark.parametrize("impl", IMPLS)
+def test_k3_full(impl):
+    """K3-shaped prefill at full size (H=96, T=4096), 4 sampled heads."""
+    dev = _cuda()
+    inp = inputs.k3(dev)
+    _check(inp, impl, TOL_BF16, heads=[0, 31, 64, 95])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_varlen_full(impl):
+    """8 packed sequences of 1024..16384 tokens, 2 sampled heads, all sequences."""
+    dev = _cuda()
+    inp = inputs.varlen(dev)
+    _check(inp, impl, TOL_BF16, heads=[7, 88], max_seqlen=max(inp.meta["lengths"]))
+
+
+def test_decode_full():
+    """64 sequences x 96 heads, 256 steps in place; 3 sequences checked."""
+    dev = _cuda()
+    di = inputs.decode(dev)
+    S = di.S.clone()
+    pick = [0, 17, 63]
+    S_ref = di.S[pick].cpu().double().numpy()
+    max_err = 0.0
+    for t in range(di.q.shape[0]):
+        o = kda.kda_decode_step(di.q[t], di.k[t], di.v[t], di.log_alpha[t], di.beta[t], S)
+        o_ref, S_ref = oracle.decode_step(di.q[t, pick].cpu(), di.k[t, pick].cpu(),
+                                          di.v[t, pick].cpu(), di.log_alpha[t, pick].cpu(),
+                                          di.beta[t, pick].cpu(), S_ref)
+        if t % 32 == 31:
+            torch.cuda.synchronize()
+            m, _ = assert_close(o[pick], o_ref, TOL_BF16, f"decode o step {t}")
+            max_err = max(max_err, m)
+    torch.cuda.synchronize()
+    assert_close(S[pick], S_ref, TOL_BF16, "decode S after 256 steps")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_extreme_full(impl):
+    """Decay-extreme prefill at full size (T=262144), 16 sampled heads."""
+    dev = _cuda()
+    inp = inputs.extreme(dev)
+    heads = list(range(0, 96, 6))
+    _check(inp, impl, TOL_BF16, heads=heads)
