@@ -1,0 +1,461 @@
+"""Benchmark of the KDA layer core on GB300.
+
+One JSON line on rank 0.  A step is one ``kda_prefill`` call on the
+K3-shaped layer workload (B=1, H=96, T=4096, d_k=d_v=128, bf16 q/k/v/beta/
+gate, fp32 log alpha and states, gated RMSNorm output): every prefill row of
+the hot path (prologue, decay rescale, Gram, UT solve, W/U, state chain,
+output, epilogue).  ``value`` is prefill tokens/s over all ranks with inputs
+resident in HBM; the one-token decode step (64 sequences x 96 heads, state in
+place) is measured in the same run and reported under ``decode``.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU runs are independent replicas (the path has no exchange step): each
+rank runs the same workload, ``value`` = total tokens / max-over-ranks time.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA tokens/s (prefill, decode) on 1 GB300; % tensor-core / % HBM roofline"
+WORKLOAD = "k3-prefill: B=1, H=96, T=4096, d_k=d_v=128, bf16 q/k/v/beta/gate, fp32 log-alpha " \
+           "and state, gated per-head RMSNorm output"
+H, T, D = 96, 4096, 128
+# algorithmic bytes per (token, head): q, k, v, gate, y (bf16, 256 B each),
+# log alpha (fp32, 512 B), beta (bf16, 2 B); plus the state read and written once
+BYTES_PER_TOKEN_HEAD = 5 * 2 * D + 4 * D + 2
+STATE_BYTES = 4 * D * D
+DEC_N, DEC_STEPS = 64, 256
+# decode: state read + write per (sequence, head) and the token's inputs/outputs
+DEC_BYTES_PER_UNIT = 2 * STATE_BYTES + 4 * 2 * D + 4 * D + 2
+
+
+def prefill_bytes(T_=T, H_=H, N_=1):
+    return BYTES_PER_TOKEN_HEAD * T_ * H_ + 2 * STATE_BYTES * H_ * N_
+
+
+def prefill_flops(chunk: int, T_=T, H_=H, d=D):
+    """Algorithmic flops of the chunked form per call: 6 d^2 + 4 C d + C^2/3
+    per (token, head) (triangle-aware count of the chunk algebra)."""
+    return (6 * d * d + 4 * chunk * d + chunk * chunk / 3.0) * T_ * H_
+
+
+# DRAM bytes (read + write) per launch from an ncu capture of the kernel as it
+# stands (profiles/ holds the summaries); None until captured after a change.
+TRAFFIC: dict[str, float | None] = {}
+
+
+def kernel_plan(path: str, chunk: int):
+    """(kernel, roofline bound, algorithmic bytes, algorithmic flops) per launch
+    of one prefill call, in launch order."""
+    if path == "simt":
+        return [("prefill_simt_kernel<128,bf16>", "hbm", prefill_bytes(), prefill_flops(16))]
+    raise ValueError(f"no kernel plan for path {path}")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "src": "fallback"}
+
+
+# ------------------------------------------------------------------ dist
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl" if __import__("torch").cuda.is_available() else "gloo"
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    dev = torch.device("cuda") if torch.cuda.is_available() else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sms, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    mx = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["no samples"]}
+        loaded = [s for s in sms if s > 0.5 * max(sms)]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local, dist):
+    import torch
+
+    from linear_attention_recurrence_prefill_gb300 import inputs, kda
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    kda.load()
+
+    inp = inputs.k3(dev)
+    opt = dict(gate=inp.gate, impl=args.path)
+    # outputs and workspace allocated once, outside the timed region
+    o = torch.empty_like(inp.q)
+    S_T = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    o_opts = kda.kda_options_init(impl=kda.IMPLS[args.path])
+    ws_bytes = kda.kda_prefill_workspace_size(T, 1, H, D, D, o_opts)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    path, launches, chunk = kda.kda_prefill_path(T, 1, H, D, D, kda.KDA_BF16, o_opts)
+    kernels = kernel_plan(path, chunk)
+    assert len(kernels) == launches, (kernels, launches)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0, None, 1, o, S_T,
+                        workspace=ws if ws_bytes else None, phase_events=events, **opt)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if kda.kda_get_last_error() != kda.KDA_OK:
+        raise RuntimeError("device status word set during warm-up")
+
+    # --- device-timed region (inputs resident; 688 MB of inputs > L2) ---
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms_max = max_over_ranks(dist, ms)
+    clocks = clk.summary()
+
+    # --- per-kernel durations: events the library records around each of its
+    # kernels on the launching stream, over a second pass of the same steps ---
+    per = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)]
+           for _ in range(args.steps)]
+    for evs in per:        # torch creates the CUDA event on first record
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for evs in per:
+        step(evs)
+    torch.cuda.synchronize()
+    kern_ms = {}
+    for i, (name, *_rest) in enumerate(kernels):
+        kern_ms[name] = statistics.mean(evs[i].elapsed_time(evs[i + 1]) for evs in per)
+    dom_i = max(range(launches), key=lambda i: kern_ms[kernels[i][0]])
+    dom, dom_bound, dom_bytes, dom_flops = kernels[dom_i]
+    dom_ms = kern_ms[dom]
+
+    # --- end to end through the public API with host buffers ---
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in
+            ("q", "k", "v", "log_alpha", "beta", "gate", "S0")}
+    devb = {n: torch.empty_like(getattr(inp, n)) for n in host}
+    y_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    st_host = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = y_host.numel() * y_host.element_size() + st_host.numel() * st_host.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            devb[n].copy_(t, non_blocking=True)
+        kda.kda_prefill(devb["q"], devb["k"], devb["v"], devb["log_alpha"], devb["beta"],
+                        devb["S0"], None, 1, o, S_T, gate=devb["gate"], impl=args.path,
+                        workspace=ws if ws_bytes else None)
+        y_host.copy_(o, non_blocking=True)
+        st_host.copy_(S_T, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / e2e_steps)
+    del host, devb
+
+    # --- decode (state in place; 805 MB of state > L2) ---
+    dec = run_decode(args, dev, stream, dist, peaks)
+
+    # --- CPU baseline (oracle) on rank 0 at N=1 ---
+    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
+
+    if rank != 0:
+        return None
+    tokens = T * world
+    value = tokens / (ms_max / 1e3)
+    if dom_bound == "tensor":
+        achieved = dom_flops / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
+    else:
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof.update({"traffic": TRAFFIC.get(dom), "kernel": dom, "kernel_ms": dom_ms,
+                 "algorithmic_bytes": dom_bytes, "algorithmic_flops": dom_flops,
+                 "peak_src": "of measured (MEASURED_PEAKS.json, burst)"
+                 if peaks["src"] == "measured" else "of fallback"})
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T, "heads": H,
+                   "head_dim": D, "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   "path": path, "chunk": chunk,
+                   "l2": "inputs larger than L2 (688 MB of token inputs per step)"},
+        "prefill": {"hbm_gbs_algorithmic": prefill_bytes() / (ms_max / 1e3) / 1e9,
+                    "hbm_frac": prefill_bytes() / (ms_max / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    "tflops_algorithmic": prefill_flops(chunk) / (ms_max / 1e3) / 1e12,
+                    "kernel_ms": kern_ms},
+        "roofline": roof,
+        "decode": dec,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": launches * args.steps,
+    }
+    return line
+
+
+def run_decode(args, dev, stream, dist, peaks):
+    import torch
+
+    from linear_attention_recurrence_prefill_gb300 import inputs, kda
+
+    di = inputs.decode(dev)
+    S = di.S.clone()
+    o = torch.empty((DEC_N, H, D), dtype=torch.bfloat16, device=dev)
+
+    def steps(n):
+        for t in range(n):
+            kda.kda_decode_step(di.q[t], di.k[t], di.v[t], di.log_alpha[t], di.beta[t], S, o)
+
+    steps(8)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, min(args.steps, 3))
+    times = []
+    for _ in range(reps):
+        barrier(dist)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        steps(DEC_STEPS)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        times.append(ev0.elapsed_time(ev1))
+    ms = max_over_ranks(dist, statistics.median(times))
+    per_step_ms = ms / DEC_STEPS
+    bytes_step = DEC_BYTES_PER_UNIT * DEC_N * H
+    gbs = bytes_step / (per_step_ms / 1e3) / 1e9
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    del di, S
+    return {"metric": "KDA decode tokens/s (64 sequences x 96 heads, 256 steps, state in place)",
+            "value": DEC_N * DEC_STEPS * world / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": per_step_ms,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": bytes_step,
+                         "kernel": "decode_kernel<128,bf16>", "traffic": None},
+            "gpu_launches": DEC_STEPS * reps}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _oracle_step(inp, heads):
+    import oracle
+    sl = lambda t: t[:, :heads].contiguous()  # noqa: E731
+    t0 = time.perf_counter()
+    o, _ = oracle.prefill(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.log_alpha), sl(inp.beta),
+                          inp.S0[:, :heads].contiguous())
+    oracle.gated_rmsnorm(o, sl(inp.gate))
+    return time.perf_counter() - t0
+
+
+def _calibrated_heads(inp, target_s: float) -> int:
+    """Heads per oracle step so that one step takes about target_s seconds."""
+    probe = min(H, max(4, cpu_cores()))
+    dt = _oracle_step(inp, probe)
+    return max(1, min(H, int(probe * target_s / max(dt, 1e-3))))
+
+
+def cpu_baseline(args):
+    """The oracle, as it stands, on the prefill workload (all OpenMP threads):
+    every token of the first `heads` heads, `heads` chosen so that the sample
+    is about 10 s of CPU work (all 96 heads when that fits)."""
+    from linear_attention_recurrence_prefill_gb300 import inputs
+
+    inp = inputs.k3("cpu")
+    heads = _calibrated_heads(inp, args.cpu_seconds)
+    dt = _oracle_step(inp, heads)
+    return {"value": heads * T / H / dt, "unit": "tokens/s", "cores": cpu_cores(),
+            "kind": "oracle",
+            "sample": f"k3 workload, all {T} tokens of the first {heads} of {H} heads "
+                      f"({heads * T} head-tokens, {dt:.1f} s); tokens/s = head-tokens/s / {H}",
+            "seconds": dt}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the oracle timed on the host cores, W warm-up and K timed
+    steps, each step the same bounded sample of the workload."""
+    if rank != 0:
+        return None
+    from linear_attention_recurrence_prefill_gb300 import inputs
+
+    inp = inputs.k3("cpu")
+    per_step = max(1.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    heads = _calibrated_heads(inp, per_step)
+    for _ in range(args.warmup):
+        _oracle_step(inp, heads)
+    times = [_oracle_step(inp, heads) for _ in range(args.steps)]
+    dt = statistics.mean(times)
+    value = heads * T / H / dt
+    sample = (f"k3 workload, all {T} tokens of the first {heads} of {H} heads per step "
+              f"({heads * T} head-tokens); tokens/s = head-tokens/s / {H}")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": T / value * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": T, "heads": H,
+                   "head_dim": D, "parallelism": "host cores (OpenMP)",
+                   "note": "CPU oracle (token-by-token fp64 recurrence)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["auto", "simt", "tc"], default="auto",
+                    help="prefill implementation inside libkda (default: auto)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target seconds of CPU work for the oracle sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    dist = init_dist(world)
+    line = run_ours(args, rank, world, local, dist)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -22,7 +22,8 @@
  *     cu_seqlens[n] .. cu_seqlens[n+1]-1.
  *   - dtype selects the element type of q, k, v, beta, gate and o/y:
  *     KDA_F32 or KDA_BF16.  log_alpha, the states and norm_weight are always
- *     fp32.  Pointers must be 16-byte aligned.
+ *     fp32.  Pointers must be 16-byte aligned, except beta, which only needs
+ *     the alignment of its element type.
  *   - Work is enqueued on `stream` and returns before it finishes.  A negative
  *     return value means the arguments were rejected and NOTHING was launched.
  *     Errors that can only be seen on the device (a bounded wait that gave up)
@@ -48,7 +49,7 @@ enum {
   KDA_ERR_ARG = -1,         /* null pointer, bad option or count           */
   KDA_ERR_SHAPE = -2,       /* sizes inconsistent or cu_seqlens malformed   */
   KDA_ERR_DTYPE = -3,       /* unknown dtype code                           */
-  KDA_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned             */
+  KDA_ERR_ALIGN = -4,       /* a pointer is not aligned as required         */
   KDA_ERR_UNSUPPORTED = -5, /* head size or option combination not built    */
   KDA_ERR_CUDA = -6,        /* the CUDA runtime reported an error           */
   KDA_ERR_TIMEOUT = -7,     /* a bounded device-side wait gave up           */
@@ -86,6 +87,9 @@ typedef struct kda_options {
   int debug_timeout;     /* test hook: 1 = the first bounded device wait gives up
                             immediately and reports KDA_ERR_TIMEOUT              */
   long long timeout_spins; /* spin limit of bounded device waits, 0 = default   */
+  void* const* phase_events; /* NULL, or (launches + 1) cudaEvent_t handles that
+                            kda_prefill records on `stream` before each of its
+                            kernels and after the last (per-kernel timing)      */
 } kda_options;
 
 /* Fill *opt with the defaults listed above. */
@@ -125,6 +129,15 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
  * (0 when the selected path needs none). */
 size_t kda_prefill_workspace_size(int T_total, int N, int H, int d_k, int d_v,
                                   const kda_options* opt);
+
+/*
+ * The implementation kda_prefill runs for these sizes and options: returns
+ * KDA_IMPL_SIMT or KDA_IMPL_TC (> 0), or a negative status if kda_prefill
+ * would reject them.  *launches (if not NULL) receives the number of kernels
+ * one call enqueues, *chunk (if not NULL) the chunk length it uses.
+ */
+int kda_prefill_path(int T_total, int N, int H, int d_k, int d_v, int dtype,
+                     const kda_options* opt, int* launches, int* chunk);
 
 /*
  * kda_decode_step -- one recurrent token for N independent sequences, with the

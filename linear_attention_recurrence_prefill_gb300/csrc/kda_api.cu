@@ -30,6 +30,10 @@ using namespace kda;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// beta is read one element at a time: element alignment is enough
+bool beta_aligned(const void* p, int dtype) {
+  return (reinterpret_cast<uintptr_t>(p) & (dtype == KDA_BF16 ? 1u : 3u)) == 0;
+}
 bool supported_d(int d) { return d == 32 || d == 64 || d == 128; }
 
 const kda_options* opts_or_default(const kda_options* opt, kda_options* storage) {
@@ -85,7 +89,7 @@ const char* kda_status_string(int s) {
     case KDA_ERR_ARG: return "invalid argument";
     case KDA_ERR_SHAPE: return "inconsistent sizes";
     case KDA_ERR_DTYPE: return "unknown dtype";
-    case KDA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case KDA_ERR_ALIGN: return "pointer not aligned as required";
     case KDA_ERR_UNSUPPORTED: return "unsupported head size or option";
     case KDA_ERR_CUDA: return "CUDA runtime error";
     case KDA_ERR_TIMEOUT: return "a bounded device wait gave up";
@@ -104,6 +108,23 @@ size_t kda_prefill_workspace_size(int T_total, int N, int H, int d_k, int d_v,
   return tc_workspace_bytes(T_total, N, H, d_k, o);
 }
 
+int kda_prefill_path(int T_total, int N, int H, int d_k, int d_v, int dtype,
+                     const kda_options* opt, int* launches, int* chunk) {
+  kda_options def;
+  const kda_options* op = opts_or_default(opt, &def);
+  if (N < 1 || H < 1 || T_total < 0) return KDA_ERR_SHAPE;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+  if (op->chunk != 0 && op->chunk != 16 && op->chunk != 64) return KDA_ERR_ARG;
+  const int rc = check_common_opts(op);
+  if (rc != KDA_OK) return rc;
+  const int path = prefill_path(op, d_k, dtype);
+  if (path < 0 || (path == KDA_IMPL_SIMT && op->chunk == 64)) return KDA_ERR_UNSUPPORTED;
+  if (launches) *launches = path == KDA_IMPL_TC ? tc_launches(T_total, N, H, d_k, op) : 1;
+  if (chunk) *chunk = path == KDA_IMPL_TC ? tc_chunk(op) : 16;
+  return path;
+}
+
 int kda_prefill(const void* q, const void* k, const void* v, const float* log_alpha,
                 const void* beta, const float* S0, const int32_t* cu_seqlens, int N, void* o,
                 float* S_T, int T_total, int H, int d_k, int d_v, int dtype,
@@ -119,9 +140,10 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
   if (!cu_seqlens && (T_total % N) != 0) return KDA_ERR_SHAPE;
   if (op->max_seqlen < 0 || op->max_seqlen > T_total) return KDA_ERR_SHAPE;
   if (op->chunk != 0 && op->chunk != 16 && op->chunk != 64) return KDA_ERR_ARG;
-  const void* ptrs[] = {q, k, v, log_alpha, beta, o, S_T};
+  const void* ptrs[] = {q, k, v, log_alpha, o, S_T};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  if (beta && !beta_aligned(beta, dtype)) return KDA_ERR_ALIGN;
   if ((S0 && !aligned16(S0)) || (cu_seqlens && !aligned16(cu_seqlens))) return KDA_ERR_ALIGN;
   int rc = check_common_opts(op);
   if (rc != KDA_OK) return rc;
@@ -153,7 +175,10 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
     if (!aligned16(op->workspace)) return KDA_ERR_ALIGN;
     e = launch_prefill_tc(a, op, s);
   } else {
+    cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(op->phase_events);
+    if (ev && cudaEventRecord(ev[0], s) != cudaSuccess) return KDA_ERR_CUDA;
     e = launch_prefill_simt(a, dtype, s);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], s);
   }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -167,9 +192,10 @@ int kda_decode_step(const void* q, const void* k, const void* v, const float* lo
   if (N < 1 || H < 1) return KDA_ERR_SHAPE;
   if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
   if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
-  const void* ptrs[] = {q, k, v, log_alpha, beta, S, o};
+  const void* ptrs[] = {q, k, v, log_alpha, S, o};
   for (const void* p : ptrs)
     if (!aligned16(p)) return KDA_ERR_ALIGN;
+  if (!beta_aligned(beta, dtype)) return KDA_ERR_ALIGN;
   int rc = check_common_opts(op);
   if (rc != KDA_OK) return rc;
   if ((long long)N * H > 0x7fffffffLL) return KDA_ERR_SHAPE;

@@ -8,6 +8,9 @@ bool tc_prefill_supported(int, int, int) { return false; }
 
 size_t tc_workspace_bytes(int, int, int, int, const kda_options*) { return 0; }
 
+int tc_launches(int, int, int, int, const kda_options*) { return 0; }
+int tc_chunk(const kda_options*) { return 64; }
+
 cudaError_t launch_prefill_tc(const PrefillArgs&, const kda_options*, cudaStream_t) {
   return cudaErrorNotSupported;
 }

@@ -12,6 +12,10 @@ bool tc_prefill_supported(int d, int dtype, int chunk);
 // Workspace bytes the tensor-core path needs for these sizes.
 size_t tc_workspace_bytes(int T_total, int N, int H, int d, const kda_options* opt);
 
+// Kernels one tensor-core prefill call enqueues, and its chunk length.
+int tc_launches(int T_total, int N, int H, int d, const kda_options* opt);
+int tc_chunk(const kda_options* opt);
+
 // Enqueue the tensor-core prefill on stream s (arguments already checked).
 cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cudaStream_t s);
 

@@ -48,6 +48,7 @@ class kda_options(ctypes.Structure):
         ("impl", ctypes.c_int),
         ("debug_timeout", ctypes.c_int),
         ("timeout_spins", ctypes.c_longlong),
+        ("phase_events", ctypes.c_void_p),
     ]
 
 
@@ -58,8 +59,10 @@ class KdaError(RuntimeError):
 
 
 _LIB = None
-EXPORTS = ("kda_options_init", "kda_prefill", "kda_prefill_workspace_size", "kda_decode_step",
-           "kda_gated_rmsnorm", "kda_get_last_error", "kda_status_string", "kda_abi_version")
+EXPORTS = ("kda_options_init", "kda_prefill", "kda_prefill_workspace_size", "kda_prefill_path",
+           "kda_decode_step", "kda_gated_rmsnorm", "kda_get_last_error", "kda_status_string",
+           "kda_abi_version")
+PATH_NAMES = {1: "simt", 2: "tc"}
 
 
 def lib_path() -> str:
@@ -82,6 +85,9 @@ def load(path: str | None = None):
     lib.kda_prefill.restype = ci
     lib.kda_prefill_workspace_size.argtypes = [ci, ci, ci, ci, ci, po]
     lib.kda_prefill_workspace_size.restype = ctypes.c_size_t
+    pi = ctypes.POINTER(ctypes.c_int)
+    lib.kda_prefill_path.argtypes = [ci, ci, ci, ci, ci, ci, po, pi, pi]
+    lib.kda_prefill_path.restype = ci
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, po, vp]
     lib.kda_decode_step.restype = ci
     lib.kda_gated_rmsnorm.argtypes = [vp, vp, vp, vp, ci, ci, ci, cf, ci, vp]
@@ -170,12 +176,24 @@ def kda_prefill_workspace_size(T_total: int, N: int, H: int, d_k: int, d_v: int,
     return int(load().kda_prefill_workspace_size(T_total, N, H, d_k, d_v, ctypes.byref(o)))
 
 
+def kda_prefill_path(T_total: int, N: int, H: int, d_k: int, d_v: int, dtype: int = KDA_BF16,
+                     opt: kda_options | None = None) -> tuple[str, int, int]:
+    """(path name, kernels per call, chunk) that kda_prefill uses for these sizes."""
+    o = opt if opt is not None else kda_options_init()
+    launches, chunk = ctypes.c_int(0), ctypes.c_int(0)
+    rc = load().kda_prefill_path(T_total, N, H, d_k, d_v, dtype, ctypes.byref(o),
+                                 ctypes.byref(launches), ctypes.byref(chunk))
+    if rc < 0:
+        raise KdaError(rc, "kda_prefill_path")
+    return PATH_NAMES[rc], launches.value, chunk.value
+
+
 def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | None = None,
                 o=None, S_T=None, *, gate=None, norm_weight=None, chunk: int = 0,
                 l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
                 q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
                 workspace=None, max_seqlen: int = 0, impl="auto", debug_timeout: bool = False,
-                timeout_spins: int = 0, stream=None):
+                timeout_spins: int = 0, phase_events=None, stream=None):
     """Chunked prefill (C ``kda_prefill``).
 
     q, k, log_alpha [T, H, d_k]; v [T, H, d_v]; beta [T, H]; S0 [N, H, d_k, d_v]
@@ -197,6 +215,12 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
     impl_code = IMPLS[impl] if isinstance(impl, str) else int(impl)
     opt = _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
                 eps_norm, None, 0, max_seqlen, impl_code, debug_timeout, timeout_spins)
+    if phase_events is not None:  # list of torch.cuda.Event, (launches + 1) of them
+        if any(not e.cuda_event for e in phase_events):
+            raise ValueError("phase_events: record each event once first (torch creates "
+                             "the CUDA event lazily)")
+        ev_arr = (ctypes.c_void_p * len(phase_events))(*[e.cuda_event for e in phase_events])
+        opt.phase_events = ctypes.cast(ev_arr, ctypes.c_void_p)
     need = kda_prefill_workspace_size(T, N, H, d_k, d_v, opt)
     if need > 0:
         if workspace is None:

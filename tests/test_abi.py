@@ -41,8 +41,8 @@ def test_options_defaults():
     assert abs(o.eps_l2 - 1e-6) < 1e-12 and abs(o.eps_norm - 1e-6) < 1e-12
     assert not o.gate and not o.workspace and o.workspace_bytes == 0
     # layout of struct kda_options on LP64 (7 x 4-byte fields, 3 pointers,
-    # size_t, 3 ints, padding, long long)
-    assert ctypes.sizeof(kda.kda_options) == 88
+    # size_t, 3 ints, padding, long long, pointer)
+    assert ctypes.sizeof(kda.kda_options) == 96
     assert kda.kda_abi_version() == 1
 
 
@@ -124,6 +124,15 @@ def test_decode_and_norm_reject():
     assert lib.kda_gated_rmsnorm(A, A, None, A, 4, 2, 64, -1.0, kda.KDA_BF16,
                                  None) == kda.KDA_ERR_ARG
     assert lib.kda_gated_rmsnorm(A, A, None, A, 4, 2, 64, 1e-6, 3, None) == kda.KDA_ERR_DTYPE
+
+
+def test_prefill_path_query():
+    assert kda.kda_prefill_path(128, 1, 2, 32, 32, kda.KDA_F32,
+                                kda.kda_options_init(impl="simt")) == ("simt", 1, 16)
+    with pytest.raises(kda.KdaError):
+        kda.kda_prefill_path(128, 1, 2, 48, 48)
+    with pytest.raises(kda.KdaError):
+        kda.kda_prefill_path(128, 1, 2, 64, 64, kda.KDA_BF16, kda.kda_options_init(g_min=-7.0))
 
 
 def test_workspace_size_is_zero_for_simt():
