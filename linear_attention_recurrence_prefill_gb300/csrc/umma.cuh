@@ -4,6 +4,7 @@
 // memory.  Everything here is a direct spelling of a documented PTX form.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
