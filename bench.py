@@ -38,6 +38,7 @@ H, T, D = 96, 4096, 128
 BYTES_PER_TOKEN_HEAD = 5 * 2 * D + 4 * D + 2
 STATE_BYTES = 4 * D * D
 DEC_N, DEC_STEPS = 64, 256
+WS_BLOCK_BYTES = 74240  # tensor-core path: workspace block per (64-token chunk, head)
 # decode: state read + write per (sequence, head) and the token's inputs/outputs
 DEC_BYTES_PER_UNIT = 2 * STATE_BYTES + 4 * 2 * D + 4 * D + 2
 
@@ -62,6 +63,21 @@ def kernel_plan(path: str, chunk: int):
     of one prefill call, in launch order."""
     if path == "simt":
         return [("prefill_simt_kernel<128,bf16>", "hbm", prefill_bytes(), prefill_flops(16))]
+    if path == "tc":
+        chunks = (T // chunk) * H
+        ws = WS_BLOCK_BYTES * chunks
+        # prep: reads q, k, v, log alpha, beta; writes one operand block per (chunk, head)
+        prep_b = (3 * 2 * D + 4 * D + 2) * T * H + ws
+        # chain: reads the blocks and the gate, writes y, reads S0 and writes S_T
+        chain_b = ws + 2 * 2 * D * T * H + 2 * STATE_BYTES * H
+        # tensor-core flops issued per (chunk, head): Gram 3 x 4 x (128x16x128),
+        # W and U~ 2 x (128x64x64); chain 7 products of 128 x (64|128) x (64|128)
+        prep_f = (3 * 4 * 2 * 128 * 16 * 128 + 2 * 2 * 128 * 64 * 64) * chunks
+        chain_f = (2 * 128 * 64 * 64 + 2 * 2 * 128 * 64 * 128 + 2 * 128 * 64 * 64
+                   + 2 * 128 * 128 * 64) * chunks
+        return [("chunk_base_kernel", "hbm", 4 * 2, 0.0),
+                ("prep_kernel", "hbm", prep_b, prep_f),
+                ("chain_kernel", "hbm", chain_b, chain_f)]
     raise ValueError(f"no kernel plan for path {path}")
 
 
