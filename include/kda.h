@@ -169,6 +169,33 @@ int kda_gated_rmsnorm(const void* o, const void* gate, const float* w, void* y, 
                       int H, int d_v, float eps, int dtype, kda_stream_t stream);
 
 /*
+ * kda_prefill_noalloc -- the same prefill as kda_prefill on the tensor-core
+ * path, for callers that cannot allocate device memory: for example host code
+ * that must never call cudaMalloc while it serves requests (an allocation can
+ * synchronise the device or fail half way through a step), or runtimes that
+ * own every device byte through their own pool and forbid raw allocations.
+ * The pages have no counterpart; it is a convenience of this library.
+ *
+ * Arguments, layouts and results are those of kda_prefill, except that
+ * opt->workspace is ignored: the scratch is a fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads
+ * it until the process exits.  Only bf16 with d_k = d_v = 128 is accepted
+ * (KDA_ERR_UNSUPPORTED otherwise), and sizes whose scratch
+ * (kda_prefill_workspace_size) exceeds the array are refused with
+ * KDA_ERR_WORKSPACE before anything is launched.  Nothing is allocated.
+ *
+ * The first call on a device looks up the array's device address; make that
+ * first call before any stream capture.  All calls share the one array, so
+ * calls that can overlap on the GPU (different streams, or other threads)
+ * race: order them, e.g. on one stream.  No state carries over between calls.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u << 20)
+int kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* log_alpha,
+                        const void* beta, const float* S0, const int32_t* cu_seqlens, int N,
+                        void* o, float* S_T, int T_total, int H, int d_k, int d_v, int dtype,
+                        const kda_options* opt, kda_stream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the device status word of the
  * current device: KDA_OK, KDA_ERR_TIMEOUT (a bounded device wait gave up),
  * KDA_ERR_SHAPE (a kernel found cu_seqlens out of range and skipped that

@@ -59,7 +59,8 @@ class KdaError(RuntimeError):
 
 
 _LIB = None
-EXPORTS = ("kda_options_init", "kda_prefill", "kda_prefill_workspace_size", "kda_prefill_path",
+EXPORTS = ("kda_options_init", "kda_prefill", "kda_prefill_noalloc",
+           "kda_prefill_workspace_size", "kda_prefill_path",
            "kda_decode_step", "kda_gated_rmsnorm", "kda_get_last_error", "kda_status_string",
            "kda_abi_version")
 PATH_NAMES = {1: "simt", 2: "tc"}
@@ -97,6 +98,8 @@ def load(path: str | None = None):
     lib.kda_status_string.argtypes = [ci]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_abi_version.restype = ci
+    lib.kda_prefill_noalloc.argtypes = lib.kda_prefill.argtypes
+    lib.kda_prefill_noalloc.restype = ci
     if path == _build.LIB or _LIB is None:
         _LIB = lib
     return lib
@@ -275,3 +278,38 @@ def kda_gated_rmsnorm(o, gate, w=None, y=None, *, eps: float = 1e-6, stream=None
 def kda_get_last_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status word."""
     return int(load().kda_get_last_error(_stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | None = None,
+                        o=None, S_T=None, *, gate=None, norm_weight=None, l2norm_qk: bool = True,
+                        beta_is_logit: bool = False, g_min: float = -5.0, q_scale: float = 1.0,
+                        eps_l2: float = 1e-6, eps_norm: float = 1e-6, max_seqlen: int = 0,
+                        stream=None):
+    """Prefill with the library's built-in scratch (C ``kda_prefill_noalloc``).
+
+    For callers that must not allocate device memory: the library allocates
+    nothing for this call (pass ``o`` and ``S_T`` to allocate nothing here
+    either).  Same arguments and results as :func:`kda_prefill`; sizes whose
+    scratch exceeds 64 MiB raise KdaError(KDA_ERR_WORKSPACE)."""
+    import torch
+    _check_cuda(q, k, v, log_alpha, beta, S0, cu_seqlens, gate, norm_weight, o, S_T)
+    T, H, d_k = q.shape
+    d_v = v.shape[2]
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+    N = N or 1
+    if o is None:
+        o = torch.empty((T, H, d_v), dtype=q.dtype, device=q.device)
+    if S_T is None:
+        S_T = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    opt = _opts(gate, norm_weight, 64, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+                eps_norm, None, 0, max_seqlen, IMPLS["tc"], False, 0)
+    rc = load().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                    _ptr(S0), _ptr(cu_seqlens), N, _ptr(o), _ptr(S_T), T, H, d_k,
+                                    d_v, _dtype_code(q), ctypes.byref(opt), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_prefill_noalloc")
+    return o, S_T
