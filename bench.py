@@ -55,7 +55,13 @@ def prefill_flops(chunk: int, T_=T, H_=H, d=D):
 
 # DRAM bytes (read + write) per launch from an ncu capture of the kernel as it
 # stands (profiles/ holds the summaries); None until captured after a change.
-TRAFFIC: dict[str, float | None] = {}
+TRAFFIC: dict[str, float | None] = {
+    # profiles/prefill_tc_kernels_k3.md (dram read + write of one launch)
+    "prep_kernel": 916.566272e6,
+    "chain_kernel": 652.115968e6,
+    # profiles/decode_kernel_k3_decode.md
+    "decode_kernel<128,bf16>": 754.506752e6,
+}
 
 
 def kernel_plan(path: str, chunk: int):
@@ -365,7 +371,8 @@ def run_decode(args, dev, stream, dist, peaks):
             "ms_per_step": per_step_ms,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": bytes_step,
-                         "kernel": "decode_kernel<128,bf16>", "traffic": None},
+                         "kernel": "decode_kernel<128,bf16>",
+                         "traffic": TRAFFIC.get("decode_kernel<128,bf16>")},
             "gpu_launches": DEC_STEPS * reps}
 
 
