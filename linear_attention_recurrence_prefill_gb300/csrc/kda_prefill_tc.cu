@@ -52,7 +52,6 @@ using namespace umma;
 
 constexpr int kD = 128;          // head dimension (d_k = d_v)
 constexpr int kC = 64;           // chunk length
-constexpr int kThreads = 128;    // one thread per TMEM lane / channel
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr long long kDefaultSpins = 4000000000LL;  // ~2 s of clock cycles
 
@@ -149,37 +148,60 @@ __device__ __forceinline__ int find_seq(const int* base, int N, int gid) {
 }
 
 // ============================================================ prep kernel
+// 256 threads, about 106 KB of shared memory and at most 128 registers per
+// thread, so that two CTAs share an SM and hide each other's waits.
 // Shared memory (offsets from a 1024-aligned base):
-constexpr uint32_t kPrepAhi = 0;          // gram A operand hi [128 x 128] bf16
-constexpr uint32_t kPrepAlo = 32768;      // gram A operand lo
-constexpr uint32_t kPrepBhi = 65536;      // gram B operand hi [16 x 128] bf16
-constexpr uint32_t kPrepBlo = 69632;      // gram B operand lo
-//   after the Gram phase the same 72 KB region holds:
-constexpr uint32_t kPrepAmat = 0;         // fp32 [64][64]  Diag(beta) strictly-lower A
-constexpr uint32_t kPrepX = 16384;        // fp32 [64][64]  (I + A)^-1
-constexpr uint32_t kPrepY = 32768;        // fp32 scratch of the block solve (3 x 256)
-constexpr uint32_t kPrepT = 32768;        // T    : B [64 (t) x 64 (j)] fp16 SW128 (after Y)
-constexpr uint32_t kPrepKt = 40960;       // K~^T : A [128 (c) x 64 (j)] fp16 SW128
-constexpr uint32_t kPrepVt = 57344;       // V^T  : A [128 (c) x 64 (j)] fp16 SW128
-constexpr uint32_t kPrepStage = 73728;    // workspace image (74240 B)
-constexpr uint32_t kPrepQraw = kPrepStage + kWsStride;  // bf16 [64][128]
-constexpr uint32_t kPrepKraw = kPrepQraw + 16384;       // bf16 [64][128]
-constexpr uint32_t kPrepSmall = kPrepKraw + 16384;      // inv_q, inv_k, beta [64] fp32
+constexpr int kPrepThreads = 256;
+constexpr uint32_t kPrepQ = 0;            // q rows, bf16 [64][128] (256 B rows)
+constexpr uint32_t kPrepK = 16384;        // k rows, bf16 [64][128]
+constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
+constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
+//   Gram (per 64-channel half): A hi/lo [128 x 64] bf16 SW128, B hi/lo [16 x 64]
+constexpr uint32_t kPrepAhi = kPrepX, kPrepAlo = kPrepX + 16384;
+constexpr uint32_t kPrepBhi = kPrepX + 32768, kPrepBlo = kPrepX + 34816;
+//   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64], scratch
+constexpr uint32_t kPrepAmat = kPrepX, kPrepInv = kPrepX + 16384, kPrepY = kPrepX + 32768;
+//   W / U~ MMAs: K~^T and V^T A operands [128 x 64] fp16, T B operand [64 x 64] fp16
+constexpr uint32_t kPrepKt = kPrepX, kPrepVt = kPrepX + 16384, kPrepT = kPrepX + 32768;
+constexpr uint32_t kPrepWst = 0;          // W staging [64 x 128] fp16 SW128 (over q, k)
+constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
 
-__device__ __forceinline__ void st_half(uint8_t* base, uint32_t off, float v) {
-  *reinterpret_cast<__half*>(base + off) = __float2half_rn(v);
+__device__ __forceinline__ float ex2f(float x) {  // hardware 2^x (rel. error ~2^-22)
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-// hi/lo bf16 split of x: x ~= hi + lo with ~16 significant bits together.
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-  hi = __float2bfloat16_rn(x);
-  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+// bf16 hi/lo split of two floats: x ~= hi + lo with ~16 significant bits.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
+__device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 x = __bfloat1622float2(b[u]);
+    f[2 * u] = x.x;
+    f[2 * u + 1] = x.y;
+  }
+}
+
+__device__ __forceinline__ void ld8f(const float* p, float (&f)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_base;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -198,29 +220,49 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
   const int len = min(kC, s1 - tok0);
   if (len <= 0) return;
   const size_t H = (size_t)a.H;
+  uint8_t* ws = ws_block(t, gid, h);
 
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
   const __nv_bfloat16* beta = static_cast<const __nv_bfloat16*>(a.beta);
-
   float* s_invq = reinterpret_cast<float*>(sm + kPrepSmall);
   float* s_invk = s_invq + 64;
   float* s_beta = s_invk + 64;
-  const __nv_bfloat16* sq = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepQraw);
-  const __nv_bfloat16* sk = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepKraw);
+  float* G = reinterpret_cast<float*>(sm + kPrepG);
 
-  // ---- 1. raw q, k tiles (rows past the sequence end are zero) ----
-  for (int e = tid; e < kC * 16; e += kThreads) {
-    const int r = e >> 4, ch = e & 15;
-    uint4 vq = make_uint4(0, 0, 0, 0), vk = vq;
-    if (r < len) {
-      const size_t gi = ((size_t)(tok0 + r) * H + h) * kD + ch * 8;
-      vq = *reinterpret_cast<const uint4*>(q + gi);
-      vk = *reinterpret_cast<const uint4*>(k + gi);
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_base, 128);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = tmem_base;
+
+  // ---- 1. input rows by bulk copy (q, k 256 B, log alpha 512 B per token) ----
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(&bar_ld, (uint32_t)len * 1024u);
+    __syncwarp();
+    for (int r = lane; r < len; r += 32) {
+      const size_t row = (size_t)(tok0 + r) * H + h;
+      bulk_g2s(sm + kPrepQ + r * 256, q + row * kD, 256, &bar_ld);
+      bulk_g2s(sm + kPrepK + r * 256, k + row * kD, 256, &bar_ld);
+      bulk_g2s(sm + kPrepG + r * 512, a.log_alpha + row * kD, 512, &bar_ld);
     }
-    *reinterpret_cast<uint4*>(sm + kPrepQraw + r * 256 + ch * 16) = vq;
-    *reinterpret_cast<uint4*>(sm + kPrepKraw + r * 256 + ch * 16) = vk;
+  }
+  // rows past the sequence end: zero (an identity step)
+  for (int e = tid; e < (kC - len) * 16; e += kPrepThreads) {
+    const int r = len + (e >> 4), c16 = e & 15;
+    *reinterpret_cast<uint4*>(sm + kPrepQ + r * 256 + c16 * 16) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sm + kPrepK + r * 256 + c16 * 16) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sm + kPrepG + r * 512 + c16 * 32) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sm + kPrepG + r * 512 + c16 * 32 + 16) = make_uint4(0, 0, 0, 0);
   }
   if (tid < kC) {
     float b = 0.f;
@@ -230,96 +272,81 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
     }
     s_beta[tid] = b;
   }
-  if (tid == 0) {
-    mbar_init(&bar, 1);
-    mbar_fence_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(&tmem_base, 128);
-    tmem_relinquish();
-  }
+  uint32_t mma_phase = 0;
+  bool ok = __syncthreads_and(mbar_wait(&bar_ld, 0, t.spins));
+  if (!ok) goto fail;
 
-  // ---- 2. running log2-decay of channel `tid` (registers) ----
-  const int ch = tid;
-  float g[kC];
-  {
+  // ---- 2. running log2-decay per channel; L2 norms of the q, k rows ----
+  if (tid < kD) {
     float run = 0.f;
-    const float* la = a.log_alpha + ((size_t)tok0 * H + h) * kD + ch;
-#pragma unroll
     for (int r = 0; r < kC; ++r) {
-      float x = 0.f;
-      if (r < len) x = fminf(fmaxf(la[(size_t)r * H * kD], a.g_min), 0.f) * kLog2e;
-      run += x;
-      g[r] = run;
+      run += fminf(fmaxf(G[r * kD + tid], a.g_min), 0.f) * kLog2e;
+      G[r * kD + tid] = run;
     }
-  }
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  const uint32_t tmem = tmem_base;
-
-  // L2 norms (warp w: rows w, w+4, ...), q also carries q_scale
-  for (int r = warp; r < kC; r += 4) {
-    const __nv_bfloat162* rq = reinterpret_cast<const __nv_bfloat162*>(sq + r * kD);
-    const __nv_bfloat162* rk = reinterpret_cast<const __nv_bfloat162*>(sk + r * kD);
-    float ssq = 0.f, ssk = 0.f;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 xq = __bfloat1622float2(rq[lane * 2 + i]);
-      const float2 xk = __bfloat1622float2(rk[lane * 2 + i]);
-      ssq += xq.x * xq.x + xq.y * xq.y;
-      ssk += xk.x * xk.x + xk.y * xk.y;
-    }
-    ssq = warp_sum(ssq);
-    ssk = warp_sum(ssk);
-    if (lane == 0) {
-      float iq = 1.f, ik = 1.f;
-      if (a.l2norm_qk) {
-        iq = (ssq + a.eps_l2) > 0.f ? 1.0f / sqrtf(ssq + a.eps_l2) : 0.f;
-        ik = (ssk + a.eps_l2) > 0.f ? 1.0f / sqrtf(ssk + a.eps_l2) : 0.f;
+  } else {
+    for (int rr = warp - 4; rr < 2 * kC; rr += 4) {
+      const int r = rr & (kC - 1);
+      const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
+      const uint2 x = *reinterpret_cast<const uint2*>(src + lane * 8);
+      const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+      const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+      const float ss = warp_sum(x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y) + a.eps_l2;
+      if (lane == 0) {
+        const float inv = a.l2norm_qk ? (ss > 0.f ? 1.0f / sqrtf(ss) : 0.f) : 1.f;
+        if (rr < kC) s_invq[r] = inv * a.q_scale;
+        else s_invk[r] = inv;
       }
-      s_invq[r] = iq * a.q_scale;
-      s_invk[r] = ik;
     }
   }
   __syncthreads();
 
-  // per-tile log2 values of this channel: end of tile b
-  float gend[4];
+  // ---- 3. Gram matrices: column tile b, 64-channel half kh at a time ----
+  //   A rows r >= 16b: [k^_r ; q^_r] * 2^(g_r - gend_b);  B rows j in tile b:
+  //   k^_j * 2^(gend_b - g_j); bf16 hi/lo; D[:, 16b..16b+15] += A B^T (3 products)
+#pragma unroll 1
+  for (int round = 0; round < 8; ++round) {
+    const int b = round >> 1, kh = round & 1;
+    const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group)
+    const float* gend = G + (16 * b + 15) * kD + 64 * kh;
+    for (int it = tid; it < nA + 128; it += kPrepThreads) {
+      if (it < nA) {
+        const int r = 16 * b + (it >> 3), c8 = it & 7;
+        const int ch = 64 * kh + 8 * c8;
+        float g8[8], ge[8], kf[8], qf[8];
+        ld8f(G + r * kD + ch, g8);
+        ld8f(gend + 8 * c8, ge);
+        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
+        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
+        const float ik = s_invk[r], iq = s_invq[r];
+        uint32_t khi[4], klo[4], qhi[4], qlo[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) gend[b] = g[16 * b + 15];
-
-  // ---- 3. Gram matrices, one 16-column tile at a time ----
-  uint32_t phase = 0;
-  bool ok = true;
+        for (int u = 0; u < 4; ++u) {
+          const float e0 = ex2f(g8[2 * u] - ge[2 * u]), e1 = ex2f(g8[2 * u + 1] - ge[2 * u + 1]);
+          split2(kf[2 * u] * ik * e0, kf[2 * u + 1] * ik * e1, khi[u], klo[u]);
+          split2(qf[2 * u] * iq * e0, qf[2 * u + 1] * iq * e1, qhi[u], qlo[u]);
+        }
+        const uint32_t ok_ = sw128_chunk(r, c8, 128), oq = sw128_chunk(64 + r, c8, 128);
+        *reinterpret_cast<uint4*>(sm + kPrepAhi + ok_) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
+        *reinterpret_cast<uint4*>(sm + kPrepAlo + ok_) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
+        *reinterpret_cast<uint4*>(sm + kPrepAhi + oq) = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
+        *reinterpret_cast<uint4*>(sm + kPrepAlo + oq) = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
+      } else {
+        const int e = it - nA, jj = e >> 3, c8 = e & 7;
+        const int j = 16 * b + jj, ch = 64 * kh + 8 * c8;
+        float g8[8], ge[8], kf[8];
+        ld8f(G + j * kD + ch, g8);
+        ld8f(gend + 8 * c8, ge);
+        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + ch * 2), kf);
+        const float ik = s_invk[j];
+        uint32_t hi[4], lo[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    if (!ok) continue;
-    // B operand: K-^(b)_j = k^_j * 2^(gend_b - g_j), j in tile b   [16 x 128]
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const int j = 16 * b + jj;
-      const float x = __bfloat162float(sk[j * kD + ch]) * s_invk[j] * exp2f(gend[b] - g[j]);
-      __nv_bfloat16 hi, lo;
-      split_bf16(x, hi, lo);
-      const uint32_t off = sw128_offset(jj, ch, 16);
-      *reinterpret_cast<__nv_bfloat16*>(sm + kPrepBhi + off) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(sm + kPrepBlo + off) = lo;
-    }
-    // A operand rows r >= 16b: [K~^(b); Q~^(b)] with factor 2^(g_r - gend_b)
-#pragma unroll
-    for (int r = 16 * b; r < kC; ++r) {
-      const float e = exp2f(g[r] - gend[b]);
-      const float xk = __bfloat162float(sk[r * kD + ch]) * s_invk[r] * e;
-      const float xq = __bfloat162float(sq[r * kD + ch]) * s_invq[r] * e;
-      __nv_bfloat16 hk, lk, hq, lq;
-      split_bf16(xk, hk, lk);
-      split_bf16(xq, hq, lq);
-      const uint32_t ok_ = sw128_offset(r, ch, 128), oq = sw128_offset(64 + r, ch, 128);
-      *reinterpret_cast<__nv_bfloat16*>(sm + kPrepAhi + ok_) = hk;
-      *reinterpret_cast<__nv_bfloat16*>(sm + kPrepAlo + ok_) = lk;
-      *reinterpret_cast<__nv_bfloat16*>(sm + kPrepAhi + oq) = hq;
-      *reinterpret_cast<__nv_bfloat16*>(sm + kPrepAlo + oq) = lq;
+        for (int u = 0; u < 4; ++u)
+          split2(kf[2 * u] * ik * ex2f(ge[2 * u] - g8[2 * u]),
+                 kf[2 * u + 1] * ik * ex2f(ge[2 * u + 1] - g8[2 * u + 1]), hi[u], lo[u]);
+        const uint32_t o = sw128_chunk(jj, c8, 16);
+        *reinterpret_cast<uint4*>(sm + kPrepBhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sm + kPrepBlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
     }
     fence_proxy_async();
     fence_before_sync();
@@ -329,54 +356,47 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
       const uint32_t d = tmem + 16 * b;
       const uint32_t ahi = smem_u32(sm + kPrepAhi), alo = smem_u32(sm + kPrepAlo);
       const uint32_t bhi = smem_u32(sm + kPrepBhi), blo = smem_u32(sm + kPrepBlo);
-      int first = 1;
       const uint32_t pa[3] = {ahi, ahi, alo}, pb[3] = {bhi, blo, bhi};
       for (int p = 0; p < 3; ++p)
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
-          mma_ss(d, desc_k_sw128(pa[p] + kb * 128 * 128, kbyte),
-                 desc_k_sw128(pb[p] + kb * 16 * 128, kbyte), kIdF16Bf16, first ? 0u : 1u);
-          first = 0;
-        }
-      mma_commit(&bar);
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(d, desc_k_sw128(pa[p], ks * 32), desc_k_sw128(pb[p], ks * 32), kIdF16Bf16,
+                 (kh | p | ks) ? 1u : 0u);
+      mma_commit(&bar_mma);
     }
-    ok = mbar_wait(&bar, phase, t.spins);
-    phase ^= 1;
+    ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
+    mma_phase ^= 1;
+    if (!ok) goto fail;
     fence_after_sync();
   }
-  if (!ok) goto fail;
 
   {
-    // ---- 4. read A (lanes 0..63) and P (lanes 64..127) ----
+    // ---- 4. A (lanes 0..63) to shared memory, P (lanes 64..127) to the workspace ----
     float* Amat = reinterpret_cast<float*>(sm + kPrepAmat);
-    uint8_t* stage = sm + kPrepStage;
     {
-      uint32_t v0[32], v1[32];
-      tmem_ld32(taddr(tmem, warp * 32, 0), v0);
-      tmem_ld32(taddr(tmem, warp * 32, 32), v1);
+      const int quarter = warp & 3, chalf = warp >> 2;
+      const int r = quarter * 32 + lane;
+      uint32_t x[32];
+      tmem_ld32(taddr(tmem, quarter * 32, 32 * chalf), x);
       tmem_wait_ld();
-      if (tid < kC) {
-        const int r = tid;
+      if (r < kC) {
         const float br = s_beta[r];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          Amat[r * kC + j] = (j < r) ? br * __uint_as_float(v0[j]) : 0.f;
-          Amat[r * kC + 32 + j] = (32 + j < r) ? br * __uint_as_float(v1[j]) : 0.f;
+          const int jj = 32 * chalf + j;
+          Amat[r * kC + jj] = (jj < r) ? br * __uint_as_float(x[j]) : 0.f;
         }
       } else {
-        const int tr = tid - kC;  // output row t
+        const int tr = r - kC;
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int c8 = 0; c8 < 4; ++c8) {
           uint32_t w[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j0 = c8 * 8 + 2 * i;
-            const float p0 = (j0 <= tr) ? __uint_as_float(j0 < 32 ? v0[j0] : v1[j0 - 32]) : 0.f;
-            const float p1 =
-                (j0 + 1 <= tr) ? __uint_as_float(j0 + 1 < 32 ? v0[j0 + 1] : v1[j0 + 1 - 32]) : 0.f;
-            w[i] = pack_half2(p0, p1);
+          for (int u = 0; u < 4; ++u) {
+            const int j0 = 8 * c8 + 2 * u, jj = 32 * chalf + j0;
+            w[u] = pack_half2(jj <= tr ? __uint_as_float(x[j0]) : 0.f,
+                              jj + 1 <= tr ? __uint_as_float(x[j0 + 1]) : 0.f);
           }
-          *reinterpret_cast<uint4*>(stage + kWsP + sw128_chunk(tr, c8, 64)) =
+          *reinterpret_cast<uint4*>(ws + kWsP + sw128_chunk(tr, 4 * chalf + c8, 64)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
@@ -385,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
     __syncthreads();
 
     // ---- 5. X = (I + A)^-1 by 16 x 16 blocks, T = X Diag(beta) ----
-    float* X = reinterpret_cast<float*>(sm + kPrepX);
+    float* X = reinterpret_cast<float*>(sm + kPrepInv);
     float* Y = reinterpret_cast<float*>(sm + kPrepY);
-    for (int e = tid; e < kC * kC; e += kThreads) X[e] = 0.f;
+    for (int e = tid; e < kC * kC; e += kPrepThreads) X[e] = 0.f;
     __syncthreads();
     if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc)
       const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;
@@ -403,10 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
       for (int r = 0; r < 16; ++r) X[(o + r) * kC + o + cc] = x[r];
     }
     __syncthreads();
-    // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj
-    for (int dd = 1; dd < 4; ++dd) {
+    for (int dd = 1; dd < 4; ++dd) {  // X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj
       const int nblk = 4 - dd;
-      for (int e = tid; e < nblk * 256; e += kThreads) {
+      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
         const int bj = e >> 8, bi = bj + dd, r = (e >> 4) & 15, cc = e & 15;
         float acc = 0.f;
         for (int m = 16 * bj; m < 16 * bi; ++m)
@@ -414,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
         Y[e] = acc;
       }
       __syncthreads();
-      for (int e = tid; e < nblk * 256; e += kThreads) {
+      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
         const int bj = e >> 8, bi = bj + dd, r = (e >> 4) & 15, cc = e & 15;
         float acc = 0.f;
 #pragma unroll
@@ -424,44 +443,43 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
       }
       __syncthreads();
     }
-    // T tile [N = t][K = j] fp16: thread -> (row t, half of the columns)
-    {
-      const int tr = tid >> 1, hf = tid & 1;
-      uint8_t* T = sm + kPrepT;
+    for (int e = tid; e < kC * 8; e += kPrepThreads) {  // T tile [t][j] fp16
+      const int tr = e >> 3, c8 = e & 7;
+      uint32_t w[4];
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const int cc8 = hf * 4 + c8;
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j0 = cc8 * 8 + 2 * i;
-          w[i] = pack_half2(X[tr * kC + j0] * s_beta[j0], X[tr * kC + j0 + 1] * s_beta[j0 + 1]);
-        }
-        *reinterpret_cast<uint4*>(T + sw128_chunk(tr, cc8, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int u = 0; u < 4; ++u) {
+        const int j0 = 8 * c8 + 2 * u;
+        w[u] = pack_half2(X[tr * kC + j0] * s_beta[j0], X[tr * kC + j0 + 1] * s_beta[j0 + 1]);
       }
+      *reinterpret_cast<uint4*>(sm + kPrepT + sw128_chunk(tr, c8, 64)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
+    __syncthreads();
 
-    // ---- 6. A operands K~^T and V^T (row = channel) and the W / U~ MMAs ----
+    // ---- 6. A operands K~^T, V^T [channel][token] fp16; W^T, U~^T MMAs ----
     {
+      const int ch = tid & (kD - 1), jq = tid >> 7;  // 4 token groups of 8 per thread
+      const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepK);
       const __nv_bfloat16* vcol = v + ((size_t)tok0 * H + h) * kD + ch;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int m = 0; m < 4; ++m) {
+        const int j8 = 4 * jq + m;
         uint32_t wk[4], wv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int u = 0; u < 4; ++u) {
           float kv[2], vv[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = c8 * 8 + 2 * i + u;
-            kv[u] = __bfloat162float(sk[j * kD + ch]) * s_invk[j] * exp2f(g[j]);
-            vv[u] = (j < len) ? __bfloat162float(vcol[(size_t)j * H * kD]) : 0.f;
+          for (int z = 0; z < 2; ++z) {
+            const int j = 8 * j8 + 2 * u + z;
+            kv[z] = __bfloat162float(kr[j * kD + ch]) * s_invk[j] * ex2f(G[j * kD + ch]);
+            vv[z] = (j < len) ? __bfloat162float(vcol[(size_t)j * H * kD]) : 0.f;
           }
-          wk[i] = pack_half2(kv[0], kv[1]);
-          wv[i] = pack_half2(vv[0], vv[1]);
+          wk[u] = pack_half2(kv[0], kv[1]);
+          wv[u] = pack_half2(vv[0], vv[1]);
         }
-        *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(ch, c8, 128)) =
+        *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(ch, j8, 128)) =
             make_uint4(wk[0], wk[1], wk[2], wk[3]);
-        *reinterpret_cast<uint4*>(sm + kPrepVt + sw128_chunk(ch, c8, 128)) =
+        *reinterpret_cast<uint4*>(sm + kPrepVt + sw128_chunk(ch, j8, 128)) =
             make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
     }
@@ -473,88 +491,87 @@ __global__ void __launch_bounds__(kThreads, 1) prep_kernel(TcArgs t) {
       const uint32_t T = smem_u32(sm + kPrepT), Kt = smem_u32(sm + kPrepKt);
       const uint32_t Vt = smem_u32(sm + kPrepVt);
       for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t kbyte = ks * 32;
-        mma_ss(tmem, desc_k_sw128(Kt, kbyte), desc_k_sw128(T, kbyte), kIdF16N64, ks > 0);
-        mma_ss(tmem + 64, desc_k_sw128(Vt, kbyte), desc_k_sw128(T, kbyte), kIdF16N64, ks > 0);
+        mma_ss(tmem, desc_k_sw128(Kt, ks * 32), desc_k_sw128(T, ks * 32), kIdF16N64, ks > 0);
+        mma_ss(tmem + 64, desc_k_sw128(Vt, ks * 32), desc_k_sw128(T, ks * 32), kIdF16N64, ks > 0);
       }
-      mma_commit(&bar);
+      mma_commit(&bar_mma);
     }
-
-    // while the MMAs run: -Q~ (B [t][d_k]), K^^T (B [d_k][t]) and G_C
+    // while the MMAs run: -Q~ [t][d_k], K^^T [d_k][t] and G_C straight to the workspace
+    for (int e = tid; e < kC * 16; e += kPrepThreads) {
+      const int c8l = e & 7, tr = (e >> 3) & 63, kb = e >> 9;
+      const int ch = 64 * kb + 8 * c8l;
+      float g8[8], qf[8];
+      ld8f(G + tr * kD + ch, g8);
+      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + tr * 256 + ch * 2), qf);
+      const float iq = -s_invq[tr];
+      uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        w[u] = pack_half2(qf[2 * u] * iq * ex2f(g8[2 * u]), qf[2 * u + 1] * iq * ex2f(g8[2 * u + 1]));
+      *reinterpret_cast<uint4*>(ws + kWsQn + sw128_chunk(tr, 8 * kb + c8l, 64)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
+    }
     {
-      const float gl = g[kC - 1];
+      const int ch = tid & (kD - 1), tq = tid >> 7;
+      const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepK);
+      const float gl = G[(kC - 1) * kD + ch];
 #pragma unroll
-      for (int r = 0; r < kC; ++r) {
-        const float e = exp2f(g[r]);
-        st_half(stage + kWsQn, sw128_offset(r, ch, 64),
-                -__bfloat162float(sq[r * kD + ch]) * s_invq[r] * e);
-      }
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int m = 0; m < 4; ++m) {
+        const int t8 = 4 * tq + m;
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r0 = c8 * 8 + 2 * i;
-          const float x0 = __bfloat162float(sk[r0 * kD + ch]) * s_invk[r0] * exp2f(gl - g[r0]);
-          const float x1 =
-              __bfloat162float(sk[(r0 + 1) * kD + ch]) * s_invk[r0 + 1] * exp2f(gl - g[r0 + 1]);
-          w[i] = pack_half2(x0, x1);
+        for (int u = 0; u < 4; ++u) {
+          const int r0 = 8 * t8 + 2 * u;
+          w[u] = pack_half2(
+              __bfloat162float(kr[r0 * kD + ch]) * s_invk[r0] * ex2f(gl - G[r0 * kD + ch]),
+              __bfloat162float(kr[(r0 + 1) * kD + ch]) * s_invk[r0 + 1] *
+                  ex2f(gl - G[(r0 + 1) * kD + ch]));
         }
-        *reinterpret_cast<uint4*>(stage + kWsKh + sw128_chunk(ch, c8, 128)) =
+        *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(ch, t8, 128)) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
-      reinterpret_cast<float*>(stage + kWsGam)[ch] = exp2f(gl);
+      if (tq == 0) reinterpret_cast<float*>(ws + kWsGam)[ch] = ex2f(gl);
     }
-    ok = mbar_wait(&bar, phase, t.spins);
-    phase ^= 1;
-    fence_after_sync();
+    ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
+    mma_phase ^= 1;
     if (!ok) goto fail;
+    fence_after_sync();
 
-    // ---- 7. W (B [t][d_k], from W^T in lanes = d_k) and U~^T (A [d_v][t]) ----
+    // ---- 7. W (B [t][d_k]) via a shared-memory transpose; U~^T (A [d_v][t]) direct ----
     {
-      uint32_t v0[32], v1[32];
-      tmem_ld32(taddr(tmem, warp * 32, 0), v0);
-      tmem_ld32(taddr(tmem, warp * 32, 32), v1);
-      tmem_wait_ld();
+      const int quarter = warp & 3, chalf = warp >> 2;
+      const int ch = quarter * 32 + lane;
+      uint32_t x[32], y[32];
+      tmem_ld32(taddr(tmem, quarter * 32, 64 + 32 * chalf), x);  // U~^T[ch][t]
+      tmem_ld32(taddr(tmem, quarter * 32, 32 * chalf), y);       // W^T[ch][t]
+      tmem_wait_ld();  // t = 32 chalf + j
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        st_half(stage + kWsW, sw128_offset(j, ch, 64), __uint_as_float(v0[j]));
-        st_half(stage + kWsW, sw128_offset(32 + j, ch, 64), __uint_as_float(v1[j]));
-      }
-      tmem_ld32(taddr(tmem, warp * 32, 64), v0);
-      tmem_ld32(taddr(tmem, warp * 32, 96), v1);
-      tmem_wait_ld();
+      for (int j = 0; j < 32; ++j)
+        *reinterpret_cast<__half*>(sm + kPrepWst + sw128_offset(32 * chalf + j, ch, 64)) =
+            __float2half_rn(__uint_as_float(y[j]));
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8 = 0; c8 < 4; ++c8) {
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int j0 = c8 * 8 + 2 * i;
-          const float x0 = __uint_as_float(j0 < 32 ? v0[j0] : v1[j0 - 32]);
-          const float x1 = __uint_as_float(j0 + 1 < 32 ? v0[j0 + 1] : v1[j0 + 1 - 32]);
-          w[i] = pack_half2(x0, x1);
-        }
-        *reinterpret_cast<uint4*>(stage + kWsUt + sw128_chunk(ch, c8, 128)) =
+        for (int u = 0; u < 4; ++u)
+          w[u] = pack_half2(__uint_as_float(x[8 * c8 + 2 * u]), __uint_as_float(x[8 * c8 + 2 * u + 1]));
+        *reinterpret_cast<uint4*>(ws + kWsUt + sw128_chunk(ch, 4 * chalf + c8, 128)) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
-    fence_proxy_async();
-    fence_before_sync();
     __syncthreads();
-    if (tid == 0) {
-      bulk_s2g(ws_block(t, gid, h), stage, kWsBytes);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    for (int e = tid; e < 1024; e += kPrepThreads)
+      reinterpret_cast<uint4*>(ws + kWsW)[e] = reinterpret_cast<const uint4*>(sm + kPrepWst)[e];
   }
   goto done;
 fail:
-  // a bounded wait gave up: report, then wait (bounded) for the MMAs this CTA
-  // issued, so that TMEM is not released under them
+  // a bounded wait gave up: report, then wait (bounded) for this CTA's own
+  // copies and MMAs before releasing TMEM and shared memory
   if (tid == 0) {
     report(a.status, KDA_ERR_TIMEOUT);
-    mma_commit(&bar);
-    mbar_wait(&bar, phase, t.spins);
+    mbar_wait(&bar_ld, 0, t.spins);
+    mma_commit(&bar_mma);
+    mbar_wait(&bar_mma, mma_phase, t.spins);
   }
 done:
   fence_before_sync();
@@ -564,6 +581,13 @@ done:
 }
 
 // ============================================================ chain kernel
+// 256 threads.  Warps 0-3 carry the state: the S^T and U^T operand
+// conversions, and in thread 0 the MMA issue and the bulk loads.  Warps 4-7
+// run the epilogue from a double-buffered O^T while the next chunk's MMAs
+// run.  Warp w touches TMEM lanes 32*(w%4) .. 32*(w%4)+31 (lane = d_v index).
+// Every bounded wait is followed by a reducing barrier, so that a timeout
+// makes the whole group leave its loop together.
+constexpr int kChThreads = 256;
 constexpr uint32_t kChBuf0 = 0;
 constexpr uint32_t kChBuf1 = kWsStride;
 constexpr uint32_t kChId = 2 * kWsStride;            // identity B [64 x 64] fp16
@@ -571,16 +595,25 @@ constexpr uint32_t kChE = kChId + 8192;              // fp32 [64][kEStride] epil
 constexpr int kEStride = kD + 4;
 constexpr uint32_t kChSmem = kChE + kC * kEStride * 4 + 1024;
 
-// TMEM columns
-constexpr uint32_t kTS = 0, kTU = 128, kTO = 192, kTAS = 256, kTAU = 320;
+// TMEM columns: S^T fp32, U^T fp32, O^T fp32 (two buffers), -S^T fp16, U^T fp16
+constexpr uint32_t kTS = 0, kTU = 128, kTO0 = 192, kTAS = 320, kTAU = 384;
+constexpr uint32_t kBarState = 1, kBarEpi = 2;  // named barriers of the two groups
 
-__global__ void __launch_bounds__(kThreads, 1) chain_kernel(TcArgs t) {
+// sigmoid with the hardware exp2 / reciprocal approximations (relative error
+// a few 1e-7, far below the bf16 output rounding)
+__device__ __forceinline__ float fast_sigmoid(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+
+__global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_u, bar_s, bar_dbg;
+  __shared__ uint64_t bar_full[2], bar_u, bar_s, bar_o[2], bar_oe[2], bar_dbg;
   __shared__ uint32_t tmem_base;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = (warp & 3) * 32 + lane;  // TMEM lane of this thread = d_v index
+  const bool state_group = warp < 4;
   const PrefillArgs& a = t.a;
   const int h = blockIdx.x % a.H, n = blockIdx.x / a.H;
   const size_t H = (size_t)a.H;
@@ -596,12 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(TcArgs t) {
     mbar_init(&bar_full[1], 1);
     mbar_init(&bar_u, 1);
     mbar_init(&bar_s, 1);
+    mbar_init(&bar_o[0], 1);
+    mbar_init(&bar_o[1], 1);
+    mbar_init(&bar_oe[0], 4);  // one arrival per epilogue warp
+    mbar_init(&bar_oe[1], 4);
     mbar_init(&bar_dbg, 1);
     mbar_fence_init();
   }
   __syncthreads();
   if (t.debug_timeout) {  // test hook: a wait that nothing completes, before any async work
-    const bool ok = mbar_wait(&bar_dbg, 0, 1000);
+    const bool ok = __syncthreads_and(mbar_wait(&bar_dbg, 0, 1000));
     if (!ok && tid == 0) report(a.status, KDA_ERR_TIMEOUT);
     if (!ok) return;
   }
@@ -610,14 +647,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(TcArgs t) {
     tmem_relinquish();
   }
   // identity operand for U^T <- U~^T * I
-  for (int e = tid; e < kC * 8; e += kThreads) {
+  for (int e = tid; e < kC * 8; e += kChThreads) {
     const int r = e >> 3, c8 = e & 7;
     uint32_t w[4] = {0, 0, 0, 0};
-    if ((r >> 3) == c8) {
-      const int i = (r & 7) >> 1;
-      w[i] = (r & 1) ? 0x3C000000u : 0x00003C00u;  // fp16 1.0 in the high / low half
-    }
-    *reinterpret_cast<uint4*>(sm + kChId + sw128_chunk(r, c8, 64)) = make_uint4(w[0], w[1], w[2], w[3]);
+    if ((r >> 3) == c8) w[(r & 7) >> 1] = (r & 1) ? 0x3C000000u : 0x00003C00u;  // fp16 1.0
+    *reinterpret_cast<uint4*>(sm + kChId + sw128_chunk(r, c8, 64)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
   auto issue_load = [&](int i) {
     uint8_t* dst = sm + ((i & 1) ? kChBuf1 : kChBuf0);
@@ -626,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(TcArgs t) {
     for (int p = 0; p < kWsParts; ++p)
       bulk_g2s(dst + kWsPartOff[p], src + kWsPartOff[p], kWsPartLen[p], &bar_full[i & 1]);
   };
-  int issued = 0;  // loads issued (meaningful in thread 0)
+  int issued = 0;     // loads issued (thread 0)
   if (tid == 0) {
     for (int i = 0; i < 2 && i < nchunks; ++i) issue_load(i);
     issued = min(2, nchunks);
@@ -635,161 +670,218 @@ __global__ void __launch_bounds__(kThreads, 1) chain_kernel(TcArgs t) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t lane_base = taddr(tmem, warp * 32, 0);
-
-  // S0 -> S^T in TMEM (lane = d_v index i, column = d_k index c)
-  for (int p = 0; p < 4; ++p) {
-    uint32_t r[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      r[j] = __float_as_uint(a.S0 ? a.S0[sbase + (size_t)(32 * p + j) * kD + tid] : 0.f);
-    tmem_st32(lane_base + kTS + 32 * p, r);
-  }
-  tmem_wait_st();
-
-  const __nv_bfloat16* gate = static_cast<const __nv_bfloat16*>(a.gate);
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
-  float* E = reinterpret_cast<float*>(sm + kChE);
+  const uint32_t lane_base = taddr(tmem, (warp & 3) * 32, 0);
   bool ok = true;
-  int consumed = 0;  // chunks whose load has been waited for
-  for (int i = 0; i < nchunks && ok; ++i) {
-    const uint8_t* buf = sm + ((i & 1) ? kChBuf1 : kChBuf0);
-    ok = mbar_wait(&bar_full[i & 1], (i >> 1) & 1, t.spins);
-    if (!ok) break;
-    consumed = i + 1;
-    const float* gam = reinterpret_cast<const float*>(buf + kWsGam);
-    // -S^T (fp16) into the A operand, S^T Diag(G_C) back into the accumulator
-    for (int p = 0; p < 2; ++p) {
-      uint32_t x0[32], x1[32], pk[32];
-      tmem_ld32(lane_base + kTS + 64 * p, x0);
-      tmem_ld32(lane_base + kTS + 64 * p + 32, x1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        pk[j] = pack_half2(-__uint_as_float(x0[2 * j]), -__uint_as_float(x0[2 * j + 1]));
-        pk[16 + j] = pack_half2(-__uint_as_float(x1[2 * j]), -__uint_as_float(x1[2 * j + 1]));
-      }
-      tmem_st32(lane_base + kTAS + 32 * p, pk);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x0[j] = __float_as_uint(__uint_as_float(x0[j]) * gam[64 * p + j]);
-        x1[j] = __float_as_uint(__uint_as_float(x1[j]) * gam[64 * p + 32 + j]);
-      }
-      tmem_st32(lane_base + kTS + 64 * p, x0);
-      tmem_st32(lane_base + kTS + 64 * p + 32, x1);
-    }
-    tmem_wait_st();
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after_sync();
-      const uint32_t sb = smem_u32(buf);
-      const uint32_t id = smem_u32(sm + kChId);
-      for (int ks = 0; ks < 4; ++ks)  // U^T = U~^T I
-        mma_ss(tmem + kTU, desc_k_sw128(sb + kWsUt, ks * 32), desc_k_sw128(id, ks * 32), kIdF16N64,
-               ks > 0);
-      for (int ks = 0; ks < 8; ++ks) {  // U^T += (-S^T) W^T ;  O^T = (-S^T)(-Q~)^T
-        const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
-        mma_ts(tmem + kTU, tmem + kTAS + 8 * ks, desc_k_sw128(sb + kWsW + kb * 64 * 128, kbyte),
-               kIdF16N64, 1);
-        mma_ts(tmem + kTO, tmem + kTAS + 8 * ks, desc_k_sw128(sb + kWsQn + kb * 64 * 128, kbyte),
-               kIdF16N64, ks > 0);
-      }
-      mma_commit(&bar_u);
-    }
-    ok = mbar_wait(&bar_u, i & 1, t.spins);
-    fence_after_sync();
-    if (!ok) break;
-    {  // U^T -> fp16 A operand
-      uint32_t x0[32], x1[32], pk[32];
-      tmem_ld32(lane_base + kTU, x0);
-      tmem_ld32(lane_base + kTU + 32, x1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        pk[j] = pack_half2(__uint_as_float(x0[2 * j]), __uint_as_float(x0[2 * j + 1]));
-        pk[16 + j] = pack_half2(__uint_as_float(x1[2 * j]), __uint_as_float(x1[2 * j + 1]));
-      }
-      tmem_st32(lane_base + kTAU, pk);
-      tmem_wait_st();
-    }
-    fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      fence_after_sync();
-      const uint32_t sb = smem_u32(buf);
-      for (int ks = 0; ks < 4; ++ks) {  // O^T += U^T P^T ; S^T += U^T K^
-        mma_ts(tmem + kTO, tmem + kTAU + 8 * ks, desc_k_sw128(sb + kWsP, ks * 32), kIdF16N64, 1);
-        mma_ts(tmem + kTS, tmem + kTAU + 8 * ks, desc_k_sw128(sb + kWsKh, ks * 32), kIdF16N128, 1);
-      }
-      mma_commit(&bar_s);
-    }
-    ok = mbar_wait(&bar_s, i & 1, t.spins);
-    fence_after_sync();
-    if (!ok) break;
-    __syncthreads();
-    if (tid == 0 && i + 2 < nchunks) {
-      fence_proxy_async();
-      issue_load(i + 2);
-      issued = i + 3;
-    }
 
-    // epilogue: O^T (lane = d_v) -> E[t][d_v] -> rows of y
-    {
-      uint32_t x0[32], x1[32];
-      tmem_ld32(lane_base + kTO, x0);
-      tmem_ld32(lane_base + kTO + 32, x1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        E[j * kEStride + tid] = __uint_as_float(x0[j]);
-        E[(32 + j) * kEStride + tid] = __uint_as_float(x1[j]);
-      }
-    }
-    __syncthreads();
-    const int tok0 = s0 + i * kC;
-    const int len = min(kC, s1 - tok0);
-    for (int r = warp; r < len; r += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(&E[r * kEStride + 4 * lane]);
-      float y[4] = {x.x, x.y, x.z, x.w};
-      const size_t gi = ((size_t)(tok0 + r) * H + h) * kD + 4 * lane;
-      if (gate) {
-        const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
-        const float inv = rsqrtf(ss / kD + a.eps_norm);
-        const uint2 graw = *reinterpret_cast<const uint2*>(gate + gi);
-        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.x));
-        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&graw.y));
-        const float gg[4] = {g01.x, g01.y, g23.x, g23.y};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float nw = a.norm_weight ? a.norm_weight[4 * lane + u] : 1.f;
-          y[u] = y[u] * inv * nw * sigmoidf_(gg[u]);
-        }
-      }
-      uint2 out;
-      out.x = pack_bf162(y[0], y[1]);
-      out.y = pack_bf162(y[2], y[3]);
-      *reinterpret_cast<uint2*>(o + gi) = out;
-    }
-    __syncthreads();
-  }
-  if (!ok && tid == 0) {
-    // a bounded wait gave up: report it, then wait (bounded) for this CTA's
-    // own MMAs and bulk copies before releasing TMEM and shared memory
-    report(a.status, KDA_ERR_TIMEOUT);
-    mma_commit(&bar_dbg);
-    mbar_wait(&bar_dbg, 0, t.spins);
-    for (int j = consumed; j < issued; ++j) mbar_wait(&bar_full[j & 1], (j >> 1) & 1, t.spins);
-  }
-
-  // final state S^T -> S_T[c][i]
-  if (ok) {
+  if (state_group) {
+    // S0 -> S^T in TMEM (lane = d_v index i, column = d_k index c)
     for (int p = 0; p < 4; ++p) {
       uint32_t r[32];
-      tmem_ld32(lane_base + kTS + 32 * p, r);
-      tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) a.S_T[sbase + (size_t)(32 * p + j) * kD + tid] = __uint_as_float(r[j]);
+      for (int j = 0; j < 32; ++j)
+        r[j] = __float_as_uint(a.S0 ? a.S0[sbase + (size_t)(32 * p + j) * kD + row] : 0.f);
+      tmem_st32(lane_base + kTS + 32 * p, r);
+    }
+    tmem_wait_st();
+    int consumed = 0;
+    for (int i = 0; i < nchunks; ++i) {
+      const uint8_t* buf = sm + ((i & 1) ? kChBuf1 : kChBuf0);
+      bool w = mbar_wait(&bar_full[i & 1], (i >> 1) & 1, t.spins);
+      if (i > 0) w = w && mbar_wait(&bar_s, (i - 1) & 1, t.spins);
+      if (tid == 0 && i >= 2) w = w && mbar_wait(&bar_oe[i & 1], ((i - 2) >> 1) & 1, t.spins);
+      ok = named_sync_and(kBarState, 128, w);
+      if (!ok) break;
+      consumed = i + 1;
+      fence_after_sync();
+      if (tid == 0 && i >= 1 && i + 1 < nchunks) {  // buffer of chunk i-1 is free
+        fence_proxy_async();
+        issue_load(i + 1);
+        issued = i + 2;
+      }
+      // -S^T (fp16) into the A operand, S^T Diag(G_C) back into the accumulator
+      const float4* gam4 = reinterpret_cast<const float4*>(buf + kWsGam);
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        uint32_t x0[32], x1[32], pk[32];
+        tmem_ld32(lane_base + kTS + 64 * p, x0);
+        tmem_ld32(lane_base + kTS + 64 * p + 32, x1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pk[j] = pack_half2(-__uint_as_float(x0[2 * j]), -__uint_as_float(x0[2 * j + 1]));
+          pk[16 + j] = pack_half2(-__uint_as_float(x1[2 * j]), -__uint_as_float(x1[2 * j + 1]));
+        }
+        tmem_st32(lane_base + kTAS + 32 * p, pk);
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 g0 = gam4[16 * p + j4], g1 = gam4[16 * p + 8 + j4];
+          x0[4 * j4 + 0] = __float_as_uint(__uint_as_float(x0[4 * j4 + 0]) * g0.x);
+          x0[4 * j4 + 1] = __float_as_uint(__uint_as_float(x0[4 * j4 + 1]) * g0.y);
+          x0[4 * j4 + 2] = __float_as_uint(__uint_as_float(x0[4 * j4 + 2]) * g0.z);
+          x0[4 * j4 + 3] = __float_as_uint(__uint_as_float(x0[4 * j4 + 3]) * g0.w);
+          x1[4 * j4 + 0] = __float_as_uint(__uint_as_float(x1[4 * j4 + 0]) * g1.x);
+          x1[4 * j4 + 1] = __float_as_uint(__uint_as_float(x1[4 * j4 + 1]) * g1.y);
+          x1[4 * j4 + 2] = __float_as_uint(__uint_as_float(x1[4 * j4 + 2]) * g1.z);
+          x1[4 * j4 + 3] = __float_as_uint(__uint_as_float(x1[4 * j4 + 3]) * g1.w);
+        }
+        tmem_st32(lane_base + kTS + 64 * p, x0);
+        tmem_st32(lane_base + kTS + 64 * p + 32, x1);
+      }
+      tmem_wait_st();
+      fence_before_sync();
+      named_sync(kBarState, 128);
+      const uint32_t tO = tmem + kTO0 + 64 * (i & 1);
+      if (tid == 0) {
+        fence_after_sync();
+        const uint32_t sb = smem_u32(buf);
+        const uint32_t id = smem_u32(sm + kChId);
+        for (int ks = 0; ks < 4; ++ks)  // U^T = U~^T I
+          mma_ss(tmem + kTU, desc_k_sw128(sb + kWsUt, ks * 32), desc_k_sw128(id, ks * 32),
+                 kIdF16N64, ks > 0);
+        for (int ks = 0; ks < 8; ++ks) {  // U^T += (-S^T) W^T
+          const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
+          mma_ts(tmem + kTU, tmem + kTAS + 8 * ks, desc_k_sw128(sb + kWsW + kb * 64 * 128, kbyte),
+                 kIdF16N64, 1);
+        }
+        mma_commit(&bar_u);
+        for (int ks = 0; ks < 8; ++ks) {  // O^T = (-S^T)(-Q~)^T
+          const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
+          mma_ts(tO, tmem + kTAS + 8 * ks, desc_k_sw128(sb + kWsQn + kb * 64 * 128, kbyte),
+                 kIdF16N64, ks > 0);
+        }
+      }
+      ok = named_sync_and(kBarState, 128, mbar_wait(&bar_u, i & 1, t.spins));
+      if (!ok) break;
+      fence_after_sync();
+      {  // U^T -> fp16 A operand
+        uint32_t x0[32], x1[32], pk[32];
+        tmem_ld32(lane_base + kTU, x0);
+        tmem_ld32(lane_base + kTU + 32, x1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pk[j] = pack_half2(__uint_as_float(x0[2 * j]), __uint_as_float(x0[2 * j + 1]));
+          pk[16 + j] = pack_half2(__uint_as_float(x1[2 * j]), __uint_as_float(x1[2 * j + 1]));
+        }
+        tmem_st32(lane_base + kTAU, pk);
+        tmem_wait_st();
+      }
+      fence_before_sync();
+      named_sync(kBarState, 128);
+      if (tid == 0) {
+        fence_after_sync();
+        const uint32_t sb = smem_u32(buf);
+        for (int ks = 0; ks < 4; ++ks)  // S^T += U^T K^  (the critical path first)
+          mma_ts(tmem + kTS, tmem + kTAU + 8 * ks, desc_k_sw128(sb + kWsKh, ks * 32), kIdF16N128, 1);
+        for (int ks = 0; ks < 4; ++ks)  // O^T += U^T P^T
+          mma_ts(tO, tmem + kTAU + 8 * ks, desc_k_sw128(sb + kWsP, ks * 32), kIdF16N64, 1);
+        mma_commit(&bar_s);
+        mma_commit(&bar_o[i & 1]);
+      }
+    }
+    // final state S^T -> S_T[c][i]
+    if (ok && nchunks > 0)
+      ok = named_sync_and(kBarState, 128, mbar_wait(&bar_s, (nchunks - 1) & 1, t.spins));
+    if (ok) {
+      fence_after_sync();
+      for (int p = 0; p < 4; ++p) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + kTS + 32 * p, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          a.S_T[sbase + (size_t)(32 * p + j) * kD + row] = __uint_as_float(r[j]);
+      }
+    } else if (tid == 0) {
+      // a bounded wait gave up: report it, then wait (bounded) for this CTA's
+      // own MMAs and bulk copies before TMEM and shared memory are released
+      report(a.status, KDA_ERR_TIMEOUT);
+      mma_commit(&bar_dbg);
+      mbar_wait(&bar_dbg, 0, t.spins);
+      for (int j = consumed; j < issued; ++j) mbar_wait(&bar_full[j & 1], (j >> 1) & 1, t.spins);
+    }
+  } else {
+    // ---------------- epilogue warps: O^T (lane = d_v) -> E[t][d_v] -> rows of y.
+    // Two threads own one token row (64 channels each): one shuffle per row,
+    // 16-byte loads and stores, independent work across the 64 channels.
+    const int et = tid - 128;               // 0..127
+    const int er = et >> 1, eh = et & 1;     // token row, half of the channels
+    const __nv_bfloat16* gate = static_cast<const __nv_bfloat16*>(a.gate);
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
+    float* E = reinterpret_cast<float*>(sm + kChE);
+    for (int i = 0; i < nchunks; ++i) {
+      const int tok0 = s0 + i * kC;
+      const int len = min(kC, s1 - tok0);
+      const bool live = er < len;
+      const size_t gofs = ((size_t)(tok0 + er) * H + h) * kD + 64 * eh;
+      uint4 graw[8];
+      if (gate && live) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) graw[c] = *reinterpret_cast<const uint4*>(gate + gofs + 8 * c);
+      }
+      ok = named_sync_and(kBarEpi, 128, mbar_wait(&bar_o[i & 1], (i >> 1) & 1, t.spins));
+      if (!ok) {
+        if (tid == 128) report(a.status, KDA_ERR_TIMEOUT);
+        break;
+      }
+      fence_after_sync();
+      {
+        uint32_t x0[32], x1[32];
+        const uint32_t tO = lane_base + kTO0 + 64 * (i & 1);
+        tmem_ld32(tO, x0);
+        tmem_ld32(tO + 32, x1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          E[j * kEStride + row] = __uint_as_float(x0[j]);
+          E[(32 + j) * kEStride + row] = __uint_as_float(x1[j]);
+        }
+      }
+      fence_before_sync();
+      named_sync(kBarEpi, 128);
+      if (lane == 0) mbar_arrive(&bar_oe[i & 1]);  // O^T buffer may be overwritten
+      float x[64];
+      const float4* er4 = reinterpret_cast<const float4*>(&E[er * kEStride + 64 * eh]);
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v4 = er4[c];
+        x[4 * c] = v4.x; x[4 * c + 1] = v4.y; x[4 * c + 2] = v4.z; x[4 * c + 3] = v4.w;
+        ss += v4.x * v4.x + v4.y * v4.y + v4.z * v4.z + v4.w * v4.w;
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      named_sync(kBarEpi, 128);  // E is free again
+      if (!live) continue;
+      if (gate) {
+        const float inv = rsqrtf(ss * (1.0f / kD) + a.eps_norm);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw[c]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 gf = __bfloat1622float2(g2[u]);
+            x[8 * c + 2 * u] *= inv * fast_sigmoid(gf.x);
+            x[8 * c + 2 * u + 1] *= inv * fast_sigmoid(gf.y);
+          }
+        }
+        if (a.norm_weight) {
+          const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 64 * eh);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float4 w = w4[c];
+            x[4 * c] *= w.x; x[4 * c + 1] *= w.y; x[4 * c + 2] *= w.z; x[4 * c + 3] *= w.w;
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 out;
+        out.x = pack_bf162(x[8 * c], x[8 * c + 1]);
+        out.y = pack_bf162(x[8 * c + 2], x[8 * c + 3]);
+        out.z = pack_bf162(x[8 * c + 4], x[8 * c + 5]);
+        out.w = pack_bf162(x[8 * c + 6], x[8 * c + 7]);
+        *reinterpret_cast<uint4*>(o + gofs + 8 * c) = out;
+      }
     }
   }
   fence_before_sync();
@@ -844,11 +936,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
   if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return e;
   if (t.total_chunks_max > 0 && !t.debug_timeout) {
     dim3 grid((unsigned)t.total_chunks_max, (unsigned)a.H);
-    prep_kernel<<<grid, kThreads, kPrepSmem, s>>>(t);
+    prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(t);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return e;
-  chain_kernel<<<(unsigned)(a.N * a.H), kThreads, kChSmem, s>>>(t);
+  chain_kernel<<<(unsigned)(a.N * a.H), kChThreads, kChSmem, s>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[3], s)) != cudaSuccess) return e;
   return cudaSuccess;
