@@ -173,15 +173,6 @@ __device__ __forceinline__ float ex2f(float x) {  // hardware 2^x (rel. error ~2
   return y;
 }
 
-// bf16 hi/lo split of two floats: x ~= hi + lo with ~16 significant bits.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&r);
 #pragma unroll
@@ -199,9 +190,36 @@ __device__ __forceinline__ void ld8f(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// Packed two-lane fp32 arithmetic (sm_100 family): one instruction per pair.
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+      : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// bf16 hi/lo split of a pair: x ~= hi + lo with ~16 significant bits.
+__device__ __forceinline__ void split2v(float2 x, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
+  const uint32_t hb = *reinterpret_cast<const uint32_t*>(&h);
+  const float2 hf = make_float2(__uint_as_float(hb << 16), __uint_as_float(hb & 0xFFFF0000u));
+  const float2 d = sub2(x, hf);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(d.x, d.y);
+  hi = hb;
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint64_t bar_mma;
   __shared__ uint32_t tmem_base;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -232,7 +250,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   float* G = reinterpret_cast<float*>(sm + kPrepG);
 
   if (tid == 0) {
-    mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
     mbar_fence_init();
   }
@@ -245,25 +262,32 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   fence_after_sync();
   const uint32_t tmem = tmem_base;
 
-  // ---- 1. input rows by bulk copy (q, k 256 B, log alpha 512 B per token) ----
-  if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(&bar_ld, (uint32_t)len * 1024u);
-    __syncwarp();
-    for (int r = lane; r < len; r += 32) {
-      const size_t row = (size_t)(tok0 + r) * H + h;
-      bulk_g2s(sm + kPrepQ + r * 256, q + row * kD, 256, &bar_ld);
-      bulk_g2s(sm + kPrepK + r * 256, k + row * kD, 256, &bar_ld);
-      bulk_g2s(sm + kPrepG + r * 512, a.log_alpha + row * kD, 512, &bar_ld);
+  // ---- 1. input rows by 16-byte asynchronous copies (all threads): q, k rows of
+  //      256 B and log alpha rows of 512 B; rows past the sequence end are
+  //      zero-filled (an identity step) ----
+  for (int e = tid; e < kC * 64; e += kPrepThreads) {
+    const int reg = e >> 10, w = e & 1023;  // 0: q, 1: k, 2-3: log alpha
+    int r, col16;
+    uint32_t dst;
+    const char* src;
+    if (reg < 2) {
+      r = w >> 4;
+      col16 = w & 15;
+      dst = smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + col16 * 16);
+      src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q);
+    } else {
+      const int w2 = e - 2048;
+      r = w2 >> 5;
+      col16 = w2 & 31;
+      dst = smem_u32(sm + kPrepG + r * 512 + col16 * 16);
+      src = reinterpret_cast<const char*>(a.log_alpha);
     }
+    const int rr = r < len ? r : 0;
+    const size_t row = (size_t)(tok0 + rr) * H + h;
+    src += row * (reg < 2 ? 256 : 512) + (size_t)col16 * 16;
+    cp_async16(dst, src, r < len ? 16u : 0u);
   }
-  // rows past the sequence end: zero (an identity step)
-  for (int e = tid; e < (kC - len) * 16; e += kPrepThreads) {
-    const int r = len + (e >> 4), c16 = e & 15;
-    *reinterpret_cast<uint4*>(sm + kPrepQ + r * 256 + c16 * 16) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(sm + kPrepK + r * 256 + c16 * 16) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(sm + kPrepG + r * 512 + c16 * 32) = make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(sm + kPrepG + r * 512 + c16 * 32 + 16) = make_uint4(0, 0, 0, 0);
-  }
+  cp_async_commit();
   if (tid < kC) {
     float b = 0.f;
     if (tid < len) {
@@ -272,9 +296,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     }
     s_beta[tid] = b;
   }
+  cp_async_wait_all();
   uint32_t mma_phase = 0;
-  bool ok = __syncthreads_and(mbar_wait(&bar_ld, 0, t.spins));
-  if (!ok) goto fail;
+  bool ok = true;
+  __syncthreads();
 
   // ---- 2. running log2-decay per channel; L2 norms of the q, k rows ----
   if (tid < kD) {
@@ -318,12 +343,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
         const float ik = s_invk[r], iq = s_invq[r];
+        const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
         uint32_t khi[4], klo[4], qhi[4], qlo[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float e0 = ex2f(g8[2 * u] - ge[2 * u]), e1 = ex2f(g8[2 * u + 1] - ge[2 * u + 1]);
-          split2(kf[2 * u] * ik * e0, kf[2 * u + 1] * ik * e1, khi[u], klo[u]);
-          split2(qf[2 * u] * iq * e0, qf[2 * u + 1] * iq * e1, qhi[u], qlo[u]);
+          const float2 d = sub2(make_float2(g8[2 * u], g8[2 * u + 1]),
+                                make_float2(ge[2 * u], ge[2 * u + 1]));
+          const float2 e = make_float2(ex2f(d.x), ex2f(d.y));
+          split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]), mul2(e, ik2)), khi[u], klo[u]);
+          split2v(mul2(make_float2(qf[2 * u], qf[2 * u + 1]), mul2(e, iq2)), qhi[u], qlo[u]);
         }
         const uint32_t ok_ = sw128_chunk(r, c8, 128), oq = sw128_chunk(64 + r, c8, 128);
         *reinterpret_cast<uint4*>(sm + kPrepAhi + ok_) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
@@ -338,11 +366,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         ld8f(gend + 8 * c8, ge);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + ch * 2), kf);
         const float ik = s_invk[j];
+        const float2 ik2 = make_float2(ik, ik);
         uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          split2(kf[2 * u] * ik * ex2f(ge[2 * u] - g8[2 * u]),
-                 kf[2 * u + 1] * ik * ex2f(ge[2 * u + 1] - g8[2 * u + 1]), hi[u], lo[u]);
+        for (int u = 0; u < 4; ++u) {
+          const float2 d = sub2(make_float2(ge[2 * u], ge[2 * u + 1]),
+                                make_float2(g8[2 * u], g8[2 * u + 1]));
+          split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]),
+                       mul2(make_float2(ex2f(d.x), ex2f(d.y)), ik2)), hi[u], lo[u]);
+        }
         const uint32_t o = sw128_chunk(jj, c8, 16);
         *reinterpret_cast<uint4*>(sm + kPrepBhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(sm + kPrepBlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -356,11 +388,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       const uint32_t d = tmem + 16 * b;
       const uint32_t ahi = smem_u32(sm + kPrepAhi), alo = smem_u32(sm + kPrepAlo);
       const uint32_t bhi = smem_u32(sm + kPrepBhi), blo = smem_u32(sm + kPrepBlo);
-      const uint32_t pa[3] = {ahi, ahi, alo}, pb[3] = {bhi, blo, bhi};
-      for (int p = 0; p < 3; ++p)
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(d, desc_k_sw128(pa[p], ks * 32), desc_k_sw128(pb[p], ks * 32), kIdF16Bf16,
-                 (kh | p | ks) ? 1u : 0u);
+      const uint64_t dahi = desc_k_sw128(ahi, 0), dalo = desc_k_sw128(alo, 0);
+      const uint64_t dbhi = desc_k_sw128(bhi, 0), dblo = desc_k_sw128(blo, 0);
+      // a K-step of 16 elements is 32 bytes: +2 in the descriptor's address field
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(d, dahi + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, (kh | ks) ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) mma_ss(d, dahi + 2 * ks, dblo + 2 * ks, kIdF16Bf16, 1u);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) mma_ss(d, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, 1u);
       mma_commit(&bar_mma);
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
@@ -404,6 +441,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     fence_before_sync();
     __syncthreads();
 
+    // v for the V^T operand of step 6, fetched now so that the loads overlap
+    // the solve: thread (channel ch, token group jq) holds 32 values
+    const int vch = tid & (kD - 1), vjq = tid >> 7;
+    unsigned short vreg[32];
+    {
+      const unsigned short* vcol =
+          reinterpret_cast<const unsigned short*>(v) + ((size_t)tok0 * H + h) * kD + vch;
+#pragma unroll
+      for (int z = 0; z < 32; ++z) {
+        const int j = 32 * vjq + z;
+        vreg[z] = (j < len) ? vcol[(size_t)j * H * kD] : (unsigned short)0;
+      }
+    }
+
     // ---- 5. X = (I + A)^-1 by 16 x 16 blocks, T = X Diag(beta) ----
     float* X = reinterpret_cast<float*>(sm + kPrepInv);
     float* Y = reinterpret_cast<float*>(sm + kPrepY);
@@ -423,23 +474,34 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       for (int r = 0; r < 16; ++r) X[(o + r) * kC + o + cc] = x[r];
     }
     __syncthreads();
-    for (int dd = 1; dd < 4; ++dd) {  // X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj
+    // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj;
+    // each thread computes 4 adjacent columns of one row (float4 loads of X, Y)
+    for (int dd = 1; dd < 4; ++dd) {
       const int nblk = 4 - dd;
-      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-        const int bj = e >> 8, bi = bj + dd, r = (e >> 4) & 15, cc = e & 15;
-        float acc = 0.f;
-        for (int m = 16 * bj; m < 16 * bi; ++m)
-          acc += Amat[(16 * bi + r) * kC + m] * X[m * kC + 16 * bj + cc];
-        Y[e] = acc;
+      for (int e = tid; e < nblk * 64; e += kPrepThreads) {
+        const int bj = e >> 6, bi = bj + dd, r = (e >> 2) & 15, c4 = (e & 3) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* arow = Amat + (16 * bi + r) * kC;
+        for (int m = 16 * bj; m < 16 * bi; ++m) {
+          const float am = arow[m];
+          const float4 x4 = *reinterpret_cast<const float4*>(X + m * kC + 16 * bj + c4);
+          acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+        }
+        *reinterpret_cast<float4*>(Y + (bj << 8) + r * 16 + c4) = acc;
       }
       __syncthreads();
-      for (int e = tid; e < nblk * 256; e += kPrepThreads) {
-        const int bj = e >> 8, bi = bj + dd, r = (e >> 4) & 15, cc = e & 15;
-        float acc = 0.f;
+      for (int e = tid; e < nblk * 64; e += kPrepThreads) {
+        const int bj = e >> 6, bi = bj + dd, r = (e >> 2) & 15, c4 = (e & 3) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* xrow = X + (16 * bi + r) * kC + 16 * bi;
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          acc += X[(16 * bi + r) * kC + 16 * bi + m] * Y[(bj << 8) + m * 16 + cc];
-        X[(16 * bi + r) * kC + 16 * bj + cc] = -acc;
+        for (int m = 0; m < 16; ++m) {
+          const float xm = xrow[m];
+          const float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
+          acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
+        }
+        *reinterpret_cast<float4*>(X + (16 * bi + r) * kC + 16 * bj + c4) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
       __syncthreads();
     }
@@ -458,9 +520,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 
     // ---- 6. A operands K~^T, V^T [channel][token] fp16; W^T, U~^T MMAs ----
     {
-      const int ch = tid & (kD - 1), jq = tid >> 7;  // 4 token groups of 8 per thread
+      const int ch = vch, jq = vjq;  // 4 token groups of 8 per thread
       const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepK);
-      const __nv_bfloat16* vcol = v + ((size_t)tok0 * H + h) * kD + ch;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int j8 = 4 * jq + m;
@@ -472,7 +533,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           for (int z = 0; z < 2; ++z) {
             const int j = 8 * j8 + 2 * u + z;
             kv[z] = __bfloat162float(kr[j * kD + ch]) * s_invk[j] * ex2f(G[j * kD + ch]);
-            vv[z] = (j < len) ? __bfloat162float(vcol[(size_t)j * H * kD]) : 0.f;
+            vv[z] = __uint_as_float((uint32_t)vreg[8 * m + 2 * u + z] << 16);
           }
           wk[u] = pack_half2(kv[0], kv[1]);
           wv[u] = pack_half2(vv[0], vv[1]);
@@ -488,11 +549,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     __syncthreads();
     if (tid == 0) {
       fence_after_sync();
-      const uint32_t T = smem_u32(sm + kPrepT), Kt = smem_u32(sm + kPrepKt);
-      const uint32_t Vt = smem_u32(sm + kPrepVt);
+      const uint64_t dT = desc_k_sw128(smem_u32(sm + kPrepT), 0);
+      const uint64_t dKt = desc_k_sw128(smem_u32(sm + kPrepKt), 0);
+      const uint64_t dVt = desc_k_sw128(smem_u32(sm + kPrepVt), 0);
+#pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tmem, desc_k_sw128(Kt, ks * 32), desc_k_sw128(T, ks * 32), kIdF16N64, ks > 0);
-        mma_ss(tmem + 64, desc_k_sw128(Vt, ks * 32), desc_k_sw128(T, ks * 32), kIdF16N64, ks > 0);
+        mma_ss(tmem, dKt + 2 * ks, dT + 2 * ks, kIdF16N64, ks > 0);
+        mma_ss(tmem + 64, dVt + 2 * ks, dT + 2 * ks, kIdF16N64, ks > 0);
       }
       mma_commit(&bar_mma);
     }
@@ -569,7 +632,6 @@ fail:
   // copies and MMAs before releasing TMEM and shared memory
   if (tid == 0) {
     report(a.status, KDA_ERR_TIMEOUT);
-    mbar_wait(&bar_ld, 0, t.spins);
     mma_commit(&bar_mma);
     mbar_wait(&bar_mma, mma_phase, t.spins);
   }
@@ -734,21 +796,19 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       if (tid == 0) {
         fence_after_sync();
         const uint32_t sb = smem_u32(buf);
-        const uint32_t id = smem_u32(sm + kChId);
+        const uint64_t dUt = desc_k_sw128(sb + kWsUt, 0), dId = desc_k_sw128(smem_u32(sm + kChId), 0);
+        const uint64_t dW = desc_k_sw128(sb + kWsW, 0), dQn = desc_k_sw128(sb + kWsQn, 0);
+        // K-step: +2 in the descriptor address field (32 bytes); K-block of 64: +512 (8 KB)
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // U^T = U~^T I
-          mma_ss(tmem + kTU, desc_k_sw128(sb + kWsUt, ks * 32), desc_k_sw128(id, ks * 32),
-                 kIdF16N64, ks > 0);
-        for (int ks = 0; ks < 8; ++ks) {  // U^T += (-S^T) W^T
-          const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
-          mma_ts(tmem + kTU, tmem + kTAS + 8 * ks, desc_k_sw128(sb + kWsW + kb * 64 * 128, kbyte),
-                 kIdF16N64, 1);
-        }
+          mma_ss(tmem + kTU, dUt + 2 * ks, dId + 2 * ks, kIdF16N64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // U^T += (-S^T) W^T
+          mma_ts(tmem + kTU, tmem + kTAS + 8 * ks, dW + 512 * (ks >> 2) + 2 * (ks & 3), kIdF16N64, 1);
         mma_commit(&bar_u);
-        for (int ks = 0; ks < 8; ++ks) {  // O^T = (-S^T)(-Q~)^T
-          const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
-          mma_ts(tO, tmem + kTAS + 8 * ks, desc_k_sw128(sb + kWsQn + kb * 64 * 128, kbyte),
-                 kIdF16N64, ks > 0);
-        }
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // O^T = (-S^T)(-Q~)^T
+          mma_ts(tO, tmem + kTAS + 8 * ks, dQn + 512 * (ks >> 2) + 2 * (ks & 3), kIdF16N64, ks > 0);
       }
       ok = named_sync_and(kBarState, 128, mbar_wait(&bar_u, i & 1, t.spins));
       if (!ok) break;
@@ -771,10 +831,13 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       if (tid == 0) {
         fence_after_sync();
         const uint32_t sb = smem_u32(buf);
+        const uint64_t dKh = desc_k_sw128(sb + kWsKh, 0), dP = desc_k_sw128(sb + kWsP, 0);
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // S^T += U^T K^  (the critical path first)
-          mma_ts(tmem + kTS, tmem + kTAU + 8 * ks, desc_k_sw128(sb + kWsKh, ks * 32), kIdF16N128, 1);
+          mma_ts(tmem + kTS, tmem + kTAU + 8 * ks, dKh + 2 * ks, kIdF16N128, 1);
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O^T += U^T P^T
-          mma_ts(tO, tmem + kTAU + 8 * ks, desc_k_sw128(sb + kWsP, ks * 32), kIdF16N64, 1);
+          mma_ts(tO, tmem + kTAU + 8 * ks, dP + 2 * ks, kIdF16N64, 1);
         mma_commit(&bar_s);
         mma_commit(&bar_o[i & 1]);
       }
