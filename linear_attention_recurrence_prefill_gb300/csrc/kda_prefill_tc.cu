@@ -57,16 +57,16 @@ constexpr long long kDefaultSpins = 4000000000LL;  // ~2 s of clock cycles
 
 // ---- workspace block per (chunk, head): the chain kernel's operand tiles ----
 constexpr uint32_t kWsUt = 0;        // U~^T : A [128 (d_v) x 64 (t)]    fp16 SW128
-constexpr uint32_t kWsW = 16384;     // W    : B [64 (t) x 128 (d_k)]    fp16 SW128
-constexpr uint32_t kWsQn = 32768;    // -Q~  : B [64 (t) x 128 (d_k)]    fp16 SW128
+constexpr uint32_t kWsWQ = 16384;    // [W; -Q~] : B [128 (t of W, then t of -Q~) x 128 (d_k)]
+                                     //            fp16 SW128 (one operand for both products)
 constexpr uint32_t kWsKh = 49152;    // K^^T : B [128 (d_k) x 64 (t)]    fp16 SW128
 constexpr uint32_t kWsP = 65536;     // P    : B [64 (t) x 64 (j)]       fp16 SW128
 constexpr uint32_t kWsGam = 73728;   // G_C  : fp32 [128]
 constexpr uint32_t kWsBytes = 74240;
 constexpr uint32_t kWsStride = 75776;  // 1024-aligned shared-memory buffer stride
-constexpr int kWsParts = 6;
-__constant__ uint32_t kWsPartOff[kWsParts] = {kWsUt, kWsW, kWsQn, kWsKh, kWsP, kWsGam};
-__constant__ uint32_t kWsPartLen[kWsParts] = {16384, 16384, 16384, 16384, 8192, 512};
+constexpr int kWsParts = 5;
+__constant__ uint32_t kWsPartOff[kWsParts] = {kWsUt, kWsWQ, kWsKh, kWsP, kWsGam};
+__constant__ uint32_t kWsPartLen[kWsParts] = {16384, 32768, 16384, 8192, 512};
 
 constexpr uint32_t kIdF16Bf16 = idesc_f16(128, 16, true);   // Gram: M128 N16 bf16
 constexpr uint32_t kIdF16N64 = idesc_f16(128, 64, false);   // fp16, N = 64
@@ -163,7 +163,8 @@ constexpr uint32_t kPrepBhi = kPrepX + 32768, kPrepBlo = kPrepX + 34816;
 constexpr uint32_t kPrepAmat = kPrepX, kPrepInv = kPrepX + 16384, kPrepY = kPrepX + 32768;
 //   W / U~ MMAs: K~^T and V^T A operands [128 x 64] fp16, T B operand [64 x 64] fp16
 constexpr uint32_t kPrepKt = kPrepX, kPrepVt = kPrepX + 16384, kPrepT = kPrepX + 32768;
-constexpr uint32_t kPrepWst = 0;          // W staging [64 x 128] fp16 SW128 (over q, k)
+constexpr uint32_t kPrepWst = 0;          // W staging, rows 0..63 of a [128 x 128] fp16 SW128
+                                          // tile (over the q, k rows, 32 KB)
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
 
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         w[u] = pack_half2(qf[2 * u] * iq * ex2f(g8[2 * u]), qf[2 * u + 1] * iq * ex2f(g8[2 * u + 1]));
-      *reinterpret_cast<uint4*>(ws + kWsQn + sw128_chunk(tr, 8 * kb + c8l, 64)) =
+      *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(64 + tr, 8 * kb + c8l, 128)) =
           make_uint4(w[0], w[1], w[2], w[3]);
     }
     {
@@ -610,7 +611,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       tmem_wait_ld();  // t = 32 chalf + j
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        *reinterpret_cast<__half*>(sm + kPrepWst + sw128_offset(32 * chalf + j, ch, 64)) =
+        *reinterpret_cast<__half*>(sm + kPrepWst + sw128_offset(32 * chalf + j, ch, 128)) =
             __float2half_rn(__uint_as_float(y[j]));
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
@@ -623,8 +624,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       }
     }
     __syncthreads();
-    for (int e = tid; e < 1024; e += kPrepThreads)
-      reinterpret_cast<uint4*>(ws + kWsW)[e] = reinterpret_cast<const uint4*>(sm + kPrepWst)[e];
+    for (int e = tid; e < 1024; e += kPrepThreads) {  // rows 0..63 of both K-blocks
+      const int u = e < 512 ? e : e + 512;
+      reinterpret_cast<uint4*>(ws + kWsWQ)[u] = reinterpret_cast<const uint4*>(sm + kPrepWst)[u];
+    }
   }
   goto done;
 fail:
@@ -643,22 +646,30 @@ done:
 }
 
 // ============================================================ chain kernel
-// 256 threads.  Warps 0-3 carry the state: the S^T and U^T operand
-// conversions, and in thread 0 the MMA issue and the bulk loads.  Warps 4-7
-// run the epilogue from a double-buffered O^T while the next chunk's MMAs
-// run.  Warp w touches TMEM lanes 32*(w%4) .. 32*(w%4)+31 (lane = d_v index).
-// Every bounded wait is followed by a reducing barrier, so that a timeout
-// makes the whole group leave its loop together.
-constexpr int kChThreads = 256;
+// 384 threads.  Warps 0-7 carry the state (conversions split by column half,
+// thread 0 also issues the MMAs and the bulk loads); warps 8-11 run the
+// epilogue from a double-buffered O^T, overlapping the next chunk.  Warp w
+// touches TMEM lanes 32*(w%4) .. +31 (lane = d_v index).  Per chunk i:
+//   [U^T | O^T] = U~^T [I | 0]                  (4 MMAs, N = 128, no state needed)
+//   -S^T -> fp16 operand, S^T <- S^T Diag(G_C)   (state warps)
+//   [U^T | O^T] += (-S^T) [W ; -Q~]^T           (8 MMAs, N = 128)
+//   U^T -> fp16 operand                          (state warps)
+//   S^T += U^T K^ (the critical path), O^T += U^T P^T
+//   y rows from O^T                              (epilogue warps)
+// Every bounded wait is followed by a vote of the group (reducing barrier), so
+// that a timeout makes the whole group leave its loop together.
+constexpr int kChThreads = 384;
+constexpr int kChState = 256;  // state group: warps 0-7; epilogue group: warps 8-11
 constexpr uint32_t kChBuf0 = 0;
 constexpr uint32_t kChBuf1 = kWsStride;
-constexpr uint32_t kChId = 2 * kWsStride;            // identity B [64 x 64] fp16
-constexpr uint32_t kChE = kChId + 8192;              // fp32 [64][kEStride] epilogue
+constexpr uint32_t kChId = 2 * kWsStride;            // [I; 0] B operand [128 x 64] fp16
+constexpr uint32_t kChE = kChId + 16384;             // fp32 [64][kEStride] epilogue
 constexpr int kEStride = kD + 4;
 constexpr uint32_t kChSmem = kChE + kC * kEStride * 4 + 1024;
 
-// TMEM columns: S^T fp32, U^T fp32, O^T fp32 (two buffers), -S^T fp16, U^T fp16
-constexpr uint32_t kTS = 0, kTU = 128, kTO0 = 192, kTAS = 320, kTAU = 384;
+// TMEM columns: S^T fp32; [U^T | O^T] fp32 in two buffers; -S^T fp16 operand;
+// U^T fp16 operand in two buffers
+constexpr uint32_t kTS = 0, kTUO0 = 128, kTAS = 384, kTAU0 = 448;
 constexpr uint32_t kBarState = 1, kBarEpi = 2;  // named barriers of the two groups
 
 // sigmoid with the hardware exp2 / reciprocal approximations (relative error
@@ -674,8 +685,8 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = (warp & 3) * 32 + lane;  // TMEM lane of this thread = d_v index
-  const bool state_group = warp < 4;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;  // TMEM lane of this thread = d_v index
   const PrefillArgs& a = t.a;
   const int h = blockIdx.x % a.H, n = blockIdx.x / a.H;
   const size_t H = (size_t)a.H;
@@ -708,12 +719,12 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
   }
-  // identity operand for U^T <- U~^T * I
-  for (int e = tid; e < kC * 8; e += kChThreads) {
+  // [I; 0]: rows 0..63 the identity, rows 64..127 zero
+  for (int e = tid; e < 128 * 8; e += kChThreads) {
     const int r = e >> 3, c8 = e & 7;
     uint32_t w[4] = {0, 0, 0, 0};
-    if ((r >> 3) == c8) w[(r & 7) >> 1] = (r & 1) ? 0x3C000000u : 0x00003C00u;  // fp16 1.0
-    *reinterpret_cast<uint4*>(sm + kChId + sw128_chunk(r, c8, 64)) =
+    if (r < 64 && (r >> 3) == c8) w[(r & 7) >> 1] = (r & 1) ? 0x3C000000u : 0x00003C00u;
+    *reinterpret_cast<uint4*>(sm + kChId + sw128_chunk(r, c8, 128)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
   auto issue_load = [&](int i) {
@@ -723,7 +734,7 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     for (int p = 0; p < kWsParts; ++p)
       bulk_g2s(dst + kWsPartOff[p], src + kWsPartOff[p], kWsPartLen[p], &bar_full[i & 1]);
   };
-  int issued = 0;     // loads issued (thread 0)
+  int issued = 0;  // loads issued (thread 0)
   if (tid == 0) {
     for (int i = 0; i < 2 && i < nchunks; ++i) issue_load(i);
     issued = min(2, nchunks);
@@ -732,51 +743,61 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = tmem_base;
-  const uint32_t lane_base = taddr(tmem, (warp & 3) * 32, 0);
+  const uint32_t lane_base = taddr(tmem, quarter * 32, 0);
   bool ok = true;
 
-  if (state_group) {
+  if (tid < kChState) {
+    const int chalf = warp >> 2;  // column half of this state warp
     // S0 -> S^T in TMEM (lane = d_v index i, column = d_k index c)
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < 2; ++p) {
       uint32_t r[32];
+      const int c0 = 64 * chalf + 32 * p;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        r[j] = __float_as_uint(a.S0 ? a.S0[sbase + (size_t)(32 * p + j) * kD + row] : 0.f);
-      tmem_st32(lane_base + kTS + 32 * p, r);
+        r[j] = __float_as_uint(a.S0 ? a.S0[sbase + (size_t)(c0 + j) * kD + row] : 0.f);
+      tmem_st32(lane_base + kTS + c0, r);
     }
     tmem_wait_st();
     int consumed = 0;
     for (int i = 0; i < nchunks; ++i) {
       const uint8_t* buf = sm + ((i & 1) ? kChBuf1 : kChBuf0);
+      const uint32_t tUO = tmem + kTUO0 + 128 * (i & 1), tAU = kTAU0 + 32 * (i & 1);
       bool w = mbar_wait(&bar_full[i & 1], (i >> 1) & 1, t.spins);
       if (i > 0) w = w && mbar_wait(&bar_s, (i - 1) & 1, t.spins);
+      if (tid == 0 && i > 0) w = w && mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1, t.spins);
       if (tid == 0 && i >= 2) w = w && mbar_wait(&bar_oe[i & 1], ((i - 2) >> 1) & 1, t.spins);
-      ok = named_sync_and(kBarState, 128, w);
+      ok = named_sync_and(kBarState, kChState, w);
       if (!ok) break;
       consumed = i + 1;
       fence_after_sync();
-      if (tid == 0 && i >= 1 && i + 1 < nchunks) {  // buffer of chunk i-1 is free
-        fence_proxy_async();
-        issue_load(i + 1);
-        issued = i + 2;
+      if (tid == 0) {
+        if (i >= 1 && i + 1 < nchunks) {  // every MMA of chunk i-1 is done: reuse its buffer
+          fence_proxy_async();
+          issue_load(i + 1);
+          issued = i + 2;
+        }
+        // [U^T | O^T] = U~^T [I | 0]: independent of the state, start it now
+        const uint64_t dUt = desc_k_sw128(smem_u32(buf) + kWsUt, 0);
+        const uint64_t dId = desc_k_sw128(smem_u32(sm + kChId), 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) mma_ss(tUO, dUt + 2 * ks, dId + 2 * ks, kIdF16N128, ks > 0);
       }
       // -S^T (fp16) into the A operand, S^T Diag(G_C) back into the accumulator
-      const float4* gam4 = reinterpret_cast<const float4*>(buf + kWsGam);
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
+      {
+        const float4* gam4 = reinterpret_cast<const float4*>(buf + kWsGam) + 16 * chalf;
         uint32_t x0[32], x1[32], pk[32];
-        tmem_ld32(lane_base + kTS + 64 * p, x0);
-        tmem_ld32(lane_base + kTS + 64 * p + 32, x1);
+        tmem_ld32(lane_base + kTS + 64 * chalf, x0);
+        tmem_ld32(lane_base + kTS + 64 * chalf + 32, x1);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           pk[j] = pack_half2(-__uint_as_float(x0[2 * j]), -__uint_as_float(x0[2 * j + 1]));
           pk[16 + j] = pack_half2(-__uint_as_float(x1[2 * j]), -__uint_as_float(x1[2 * j + 1]));
         }
-        tmem_st32(lane_base + kTAS + 32 * p, pk);
+        tmem_st32(lane_base + kTAS + 32 * chalf, pk);
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 g0 = gam4[16 * p + j4], g1 = gam4[16 * p + 8 + j4];
+          const float4 g0 = gam4[j4], g1 = gam4[8 + j4];
           x0[4 * j4 + 0] = __float_as_uint(__uint_as_float(x0[4 * j4 + 0]) * g0.x);
           x0[4 * j4 + 1] = __float_as_uint(__uint_as_float(x0[4 * j4 + 1]) * g0.y);
           x0[4 * j4 + 2] = __float_as_uint(__uint_as_float(x0[4 * j4 + 2]) * g0.z);
@@ -786,74 +807,63 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
           x1[4 * j4 + 2] = __float_as_uint(__uint_as_float(x1[4 * j4 + 2]) * g1.z);
           x1[4 * j4 + 3] = __float_as_uint(__uint_as_float(x1[4 * j4 + 3]) * g1.w);
         }
-        tmem_st32(lane_base + kTS + 64 * p, x0);
-        tmem_st32(lane_base + kTS + 64 * p + 32, x1);
-      }
-      tmem_wait_st();
-      fence_before_sync();
-      named_sync(kBarState, 128);
-      const uint32_t tO = tmem + kTO0 + 64 * (i & 1);
-      if (tid == 0) {
-        fence_after_sync();
-        const uint32_t sb = smem_u32(buf);
-        const uint64_t dUt = desc_k_sw128(sb + kWsUt, 0), dId = desc_k_sw128(smem_u32(sm + kChId), 0);
-        const uint64_t dW = desc_k_sw128(sb + kWsW, 0), dQn = desc_k_sw128(sb + kWsQn, 0);
-        // K-step: +2 in the descriptor address field (32 bytes); K-block of 64: +512 (8 KB)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // U^T = U~^T I
-          mma_ss(tmem + kTU, dUt + 2 * ks, dId + 2 * ks, kIdF16N64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // U^T += (-S^T) W^T
-          mma_ts(tmem + kTU, tmem + kTAS + 8 * ks, dW + 512 * (ks >> 2) + 2 * (ks & 3), kIdF16N64, 1);
-        mma_commit(&bar_u);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // O^T = (-S^T)(-Q~)^T
-          mma_ts(tO, tmem + kTAS + 8 * ks, dQn + 512 * (ks >> 2) + 2 * (ks & 3), kIdF16N64, ks > 0);
-      }
-      ok = named_sync_and(kBarState, 128, mbar_wait(&bar_u, i & 1, t.spins));
-      if (!ok) break;
-      fence_after_sync();
-      {  // U^T -> fp16 A operand
-        uint32_t x0[32], x1[32], pk[32];
-        tmem_ld32(lane_base + kTU, x0);
-        tmem_ld32(lane_base + kTU + 32, x1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          pk[j] = pack_half2(__uint_as_float(x0[2 * j]), __uint_as_float(x0[2 * j + 1]));
-          pk[16 + j] = pack_half2(__uint_as_float(x1[2 * j]), __uint_as_float(x1[2 * j + 1]));
-        }
-        tmem_st32(lane_base + kTAU, pk);
+        tmem_st32(lane_base + kTS + 64 * chalf, x0);
+        tmem_st32(lane_base + kTS + 64 * chalf + 32, x1);
         tmem_wait_st();
       }
       fence_before_sync();
-      named_sync(kBarState, 128);
+      named_sync(kBarState, kChState);
+      if (tid == 0) {
+        fence_after_sync();
+        const uint64_t dWQ = desc_k_sw128(smem_u32(buf) + kWsWQ, 0);
+        // [U^T | O^T] += (-S^T) [W ; -Q~]^T.  K-step: +2 in the descriptor's
+        // address field (32 bytes); K-block of 64: +1024 (16 KB)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N128, 1);
+        mma_commit(&bar_u);
+      }
+      ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_u, i & 1, t.spins));
+      if (!ok) break;
+      fence_after_sync();
+      {  // U^T -> fp16 A operand (column half per warp)
+        uint32_t x0[32], pk[16];
+        tmem_ld32(lane_base + (tUO - tmem) + 32 * chalf, x0);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_half2(__uint_as_float(x0[2 * j]), __uint_as_float(x0[2 * j + 1]));
+        tmem_st16(lane_base + tAU + 16 * chalf, pk);
+        tmem_wait_st();
+      }
+      fence_before_sync();
+      named_sync(kBarState, kChState);
       if (tid == 0) {
         fence_after_sync();
         const uint32_t sb = smem_u32(buf);
         const uint64_t dKh = desc_k_sw128(sb + kWsKh, 0), dP = desc_k_sw128(sb + kWsP, 0);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // S^T += U^T K^  (the critical path first)
-          mma_ts(tmem + kTS, tmem + kTAU + 8 * ks, dKh + 2 * ks, kIdF16N128, 1);
+        for (int ks = 0; ks < 4; ++ks)  // S^T += U^T K^: the state chain first
+          mma_ts(tmem + kTS, tmem + tAU + 8 * ks, dKh + 2 * ks, kIdF16N128, 1);
+        mma_commit(&bar_s);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O^T += U^T P^T
-          mma_ts(tO, tmem + kTAU + 8 * ks, dP + 2 * ks, kIdF16N64, 1);
-        mma_commit(&bar_s);
+          mma_ts(tUO + 64, tmem + tAU + 8 * ks, dP + 2 * ks, kIdF16N64, 1);
         mma_commit(&bar_o[i & 1]);
       }
     }
-    // final state S^T -> S_T[c][i]
     if (ok && nchunks > 0)
-      ok = named_sync_and(kBarState, 128, mbar_wait(&bar_s, (nchunks - 1) & 1, t.spins));
-    if (ok) {
+      ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_s, (nchunks - 1) & 1, t.spins));
+    if (ok) {  // final state S^T -> S_T[c][i]
       fence_after_sync();
-      for (int p = 0; p < 4; ++p) {
+      for (int p = 0; p < 2; ++p) {
         uint32_t r[32];
-        tmem_ld32(lane_base + kTS + 32 * p, r);
+        const int c0 = 64 * chalf + 32 * p;
+        tmem_ld32(lane_base + kTS + c0, r);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          a.S_T[sbase + (size_t)(32 * p + j) * kD + row] = __uint_as_float(r[j]);
+          a.S_T[sbase + (size_t)(c0 + j) * kD + row] = __uint_as_float(r[j]);
       }
     } else if (tid == 0) {
       // a bounded wait gave up: report it, then wait (bounded) for this CTA's
@@ -865,10 +875,9 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     }
   } else {
     // ---------------- epilogue warps: O^T (lane = d_v) -> E[t][d_v] -> rows of y.
-    // Two threads own one token row (64 channels each): one shuffle per row,
-    // 16-byte loads and stores, independent work across the 64 channels.
-    const int et = tid - 128;               // 0..127
-    const int er = et >> 1, eh = et & 1;     // token row, half of the channels
+    // Two threads own one token row (64 channels each).
+    const int et = tid - kChState;            // 0..127
+    const int er = et >> 1, eh = et & 1;      // token row, half of the channels
     const __nv_bfloat16* gate = static_cast<const __nv_bfloat16*>(a.gate);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
     float* E = reinterpret_cast<float*>(sm + kChE);
@@ -884,13 +893,13 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       }
       ok = named_sync_and(kBarEpi, 128, mbar_wait(&bar_o[i & 1], (i >> 1) & 1, t.spins));
       if (!ok) {
-        if (tid == 128) report(a.status, KDA_ERR_TIMEOUT);
+        if (et == 0) report(a.status, KDA_ERR_TIMEOUT);
         break;
       }
       fence_after_sync();
       {
         uint32_t x0[32], x1[32];
-        const uint32_t tO = lane_base + kTO0 + 64 * (i & 1);
+        const uint32_t tO = lane_base + kTUO0 + 128 * (i & 1) + 64;
         tmem_ld32(tO, x0);
         tmem_ld32(tO + 32, x1);
         tmem_wait_ld();
@@ -902,56 +911,52 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       }
       fence_before_sync();
       named_sync(kBarEpi, 128);
-      if (lane == 0) mbar_arrive(&bar_oe[i & 1]);  // O^T buffer may be overwritten
-      float x[64];
+      if (lane == 0) mbar_arrive(&bar_oe[i & 1]);  // the [U|O] buffer may be overwritten
+      // pass 1: sum of squares of the row; pass 2: outputs, 8 channels at a time
       const float4* er4 = reinterpret_cast<const float4*>(&E[er * kEStride + 64 * eh]);
       float ss = 0.f;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         const float4 v4 = er4[c];
-        x[4 * c] = v4.x; x[4 * c + 1] = v4.y; x[4 * c + 2] = v4.z; x[4 * c + 3] = v4.w;
         ss += v4.x * v4.x + v4.y * v4.y + v4.z * v4.z + v4.w * v4.w;
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      named_sync(kBarEpi, 128);  // E is free again
-      if (!live) continue;
-      if (gate) {
-        const float inv = rsqrtf(ss * (1.0f / kD) + a.eps_norm);
+      const float inv = gate ? rsqrtf(ss * (1.0f / kD) + a.eps_norm) : 1.f;
+      if (live) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw[c]);
+          const float4 v0 = er4[2 * c], v1 = er4[2 * c + 1];
+          float y[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          if (gate) {
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw[c]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 gf = __bfloat1622float2(g2[u]);
-            x[8 * c + 2 * u] *= inv * fast_sigmoid(gf.x);
-            x[8 * c + 2 * u + 1] *= inv * fast_sigmoid(gf.y);
+            for (int u = 0; u < 4; ++u) {
+              const float2 gf = __bfloat1622float2(g2[u]);
+              y[2 * u] *= inv * fast_sigmoid(gf.x);
+              y[2 * u + 1] *= inv * fast_sigmoid(gf.y);
+            }
+            if (a.norm_weight) {
+              const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 64 * eh + 8 * c);
+              const float4 w0 = w4[0], w1 = w4[1];
+              y[0] *= w0.x; y[1] *= w0.y; y[2] *= w0.z; y[3] *= w0.w;
+              y[4] *= w1.x; y[5] *= w1.y; y[6] *= w1.z; y[7] *= w1.w;
+            }
           }
-        }
-        if (a.norm_weight) {
-          const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 64 * eh);
-#pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const float4 w = w4[c];
-            x[4 * c] *= w.x; x[4 * c + 1] *= w.y; x[4 * c + 2] *= w.z; x[4 * c + 3] *= w.w;
-          }
+          uint4 out;
+          out.x = pack_bf162(y[0], y[1]);
+          out.y = pack_bf162(y[2], y[3]);
+          out.z = pack_bf162(y[4], y[5]);
+          out.w = pack_bf162(y[6], y[7]);
+          *reinterpret_cast<uint4*>(o + gofs + 8 * c) = out;
         }
       }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 out;
-        out.x = pack_bf162(x[8 * c], x[8 * c + 1]);
-        out.y = pack_bf162(x[8 * c + 2], x[8 * c + 3]);
-        out.z = pack_bf162(x[8 * c + 4], x[8 * c + 5]);
-        out.w = pack_bf162(x[8 * c + 6], x[8 * c + 7]);
-        *reinterpret_cast<uint4*>(o + gofs + 8 * c) = out;
-      }
+      named_sync(kBarEpi, 128);  // E is free again
     }
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
-  (void)lane;
 }
 
 size_t header_bytes(int N) { return ((size_t)(N + 1) * 4 + 1023) & ~(size_t)1023; }
