@@ -35,6 +35,8 @@
 //   W = T K~, U~ = T V, U = U~ - W S, O = Q~ S + P U, S <- Diag(G_C) S + K^^T U.
 // For the Gram matrices the 1/G factors are taken relative to the end of the
 // column's own 16-token tile, so every factor is within e^-80 .. e^80.
+// V, K~ and K^ enter their products as MN-major operands (64-channel blocks of
+// token rows), so every one of them is produced row by row, like the inputs.
 //
 // Precision: the Gram products use a bf16 hi/lo split (hi*hi + hi*lo + lo*hi,
 // ~16 significant bits, bf16 keeps the e^+-80 range); every other product uses
@@ -59,7 +61,8 @@ constexpr long long kDefaultSpins = 4000000000LL;  // ~2 s of clock cycles
 constexpr uint32_t kWsUt = 0;        // U~^T : A [128 (d_v) x 64 (t)]    fp16 SW128
 constexpr uint32_t kWsWQ = 16384;    // [W; -Q~] : B [128 (t of W, then t of -Q~) x 128 (d_k)]
                                      //            fp16 SW128 (one operand for both products)
-constexpr uint32_t kWsKh = 49152;    // K^^T : B [128 (d_k) x 64 (t)]    fp16 SW128
+constexpr uint32_t kWsKh = 49152;    // K^   : B [128 (d_k) x 64 (t)]    fp16 SW128 MN-major
+                                     //        (64 rows t of 128 d_k, 8 KB per 64 d_k)
 constexpr uint32_t kWsP = 65536;     // P    : B [64 (t) x 64 (j)]       fp16 SW128
 constexpr uint32_t kWsGam = 73728;   // G_C  : fp32 [128]
 constexpr uint32_t kWsBytes = 74240;
@@ -71,6 +74,7 @@ __constant__ uint32_t kWsPartLen[kWsParts] = {16384, 32768, 16384, 8192, 512};
 constexpr uint32_t kIdF16Bf16 = idesc_f16(128, 16, true);   // Gram: M128 N16 bf16
 constexpr uint32_t kIdF16N64 = idesc_f16(128, 64, false);   // fp16, N = 64
 constexpr uint32_t kIdF16N128 = idesc_f16(128, 128, false); // fp16, N = 128
+constexpr uint32_t kIdKh = idesc_f16(128, 128, false, false, true);  // fp16, N = 128, B MN-major
 
 struct TcArgs {
   PrefillArgs a;
@@ -161,10 +165,13 @@ constexpr uint32_t kPrepAhi = kPrepX, kPrepAlo = kPrepX + 16384;
 constexpr uint32_t kPrepBhi = kPrepX + 32768, kPrepBlo = kPrepX + 34816;
 //   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64], scratch
 constexpr uint32_t kPrepAmat = kPrepX, kPrepInv = kPrepX + 16384, kPrepY = kPrepX + 32768;
-//   W / U~ MMAs: K~^T and V^T A operands [128 x 64] fp16, T B operand [64 x 64] fp16
-constexpr uint32_t kPrepKt = kPrepX, kPrepVt = kPrepX + 16384, kPrepT = kPrepX + 32768;
-constexpr uint32_t kPrepWst = 0;          // W staging, rows 0..63 of a [128 x 128] fp16 SW128
-                                          // tile (over the q, k rows, 32 KB)
+//   W / U~ MMAs: [T; T] [128 (t) x 64 (j)] fp16 K-major over A; V and K~ [64 (j) rows
+//   of 128 channels] fp16 MN-major over the q and k rows
+constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
+// TMEM: Gram D in columns 0..63, then U~^T (64 columns) and W (128 columns)
+constexpr uint32_t kPrepTmemCols = 256, kTdU = 0, kTdW = 64;
+constexpr uint32_t kIdUt = idesc_f16(128, 64, false, true, false);  // A MN-major, N = 64
+constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
 
@@ -255,7 +262,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(&tmem_base, 128);
+    tmem_alloc(&tmem_base, kPrepTmemCols);
     tmem_relinquish();
   }
   fence_before_sync();
@@ -442,21 +449,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     fence_before_sync();
     __syncthreads();
 
-    // v for the V^T operand of step 6, fetched now so that the loads overlap
-    // the solve: thread (channel ch, token group jq) holds 32 values
-    const int vch = tid & (kD - 1), vjq = tid >> 7;
-    unsigned short vreg[32];
-    {
-      const unsigned short* vcol =
-          reinterpret_cast<const unsigned short*>(v) + ((size_t)tok0 * H + h) * kD + vch;
+    // v rows for the V operand of step 7, fetched now so that the loads overlap
+    // the solve: item (token j, 8-channel group c16) = tid + 256 m
+    uint4 vreg[4];
 #pragma unroll
-      for (int z = 0; z < 32; ++z) {
-        const int j = 32 * vjq + z;
-        vreg[z] = (j < len) ? vcol[(size_t)j * H * kD] : (unsigned short)0;
-      }
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + kPrepThreads * m, j = e >> 4, c16 = e & 15;
+      vreg[m] = make_uint4(0u, 0u, 0u, 0u);
+      if (j < len)
+        vreg[m] = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + j) * H + h) * kD) + c16);
     }
 
-    // ---- 5. X = (I + A)^-1 by 16 x 16 blocks, T = X Diag(beta) ----
+    // ---- 5. X = (I + A)^-1 by 16 x 16 blocks ----
     float* X = reinterpret_cast<float*>(sm + kPrepInv);
     float* Y = reinterpret_cast<float*>(sm + kPrepY);
     for (int e = tid; e < kC * kC; e += kPrepThreads) X[e] = 0.f;
@@ -506,7 +510,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       }
       __syncthreads();
     }
-    for (int e = tid; e < kC * 8; e += kPrepThreads) {  // T tile [t][j] fp16
+
+    // ---- 6. [T; T] tile (K-major [t][j] fp16, rows 64..127 repeat rows 0..63) over
+    //      A; row pass: K~ and V held for step 7, -Q~ rows, K^ rows and G_C straight
+    //      to the workspace.  Row item (row r, 8-channel group c16) = tid + 256 m ----
+    for (int e = tid; e < kC * 8; e += kPrepThreads) {
       const int tr = e >> 3, c8 = e & 7;
       uint32_t w[4];
 #pragma unroll
@@ -514,119 +522,109 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         const int j0 = 8 * c8 + 2 * u;
         w[u] = pack_half2(X[tr * kC + j0] * s_beta[j0], X[tr * kC + j0 + 1] * s_beta[j0 + 1]);
       }
-      *reinterpret_cast<uint4*>(sm + kPrepT + sw128_chunk(tr, c8, 64)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
+      const uint4 wt = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(tr, c8, 128)) = wt;
+      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(kC + tr, c8, 128)) = wt;
     }
-    __syncthreads();
-
-    // ---- 6. A operands K~^T, V^T [channel][token] fp16; W^T, U~^T MMAs ----
+    uint4 ktl[4];
     {
-      const int ch = vch, jq = vjq;  // 4 token groups of 8 per thread
-      const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepK);
+      const float* Gl = G + (kC - 1) * kD;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int j8 = 4 * jq + m;
-        uint32_t wk[4], wv[4];
+        const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
+        float g8[8], gl8[8], kf[8], qf[8];
+        ld8f(G + r * kD + ch, g8);
+        ld8f(Gl + ch, gl8);
+        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
+        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
+        const float ik = s_invk[r], iq = -s_invq[r];
+        const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
+        uint32_t wk[4], wq[4], wh[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          float kv[2], vv[2];
-#pragma unroll
-          for (int z = 0; z < 2; ++z) {
-            const int j = 8 * j8 + 2 * u + z;
-            kv[z] = __bfloat162float(kr[j * kD + ch]) * s_invk[j] * ex2f(G[j * kD + ch]);
-            vv[z] = __uint_as_float((uint32_t)vreg[8 * m + 2 * u + z] << 16);
-          }
-          wk[u] = pack_half2(kv[0], kv[1]);
-          wv[u] = pack_half2(vv[0], vv[1]);
+          const float2 g2 = make_float2(g8[2 * u], g8[2 * u + 1]);
+          const float2 d = sub2(make_float2(gl8[2 * u], gl8[2 * u + 1]), g2);
+          const float2 e2 = make_float2(ex2f(g2.x), ex2f(g2.y));
+          const float2 f2 = make_float2(ex2f(d.x), ex2f(d.y));
+          const float2 k2 = mul2(make_float2(kf[2 * u], kf[2 * u + 1]), ik2);
+          const float2 q2 = mul2(make_float2(qf[2 * u], qf[2 * u + 1]), iq2);
+          const float2 kt2 = mul2(k2, e2), qt2 = mul2(q2, e2), kh2 = mul2(k2, f2);
+          wk[u] = pack_half2(kt2.x, kt2.y);
+          wq[u] = pack_half2(qt2.x, qt2.y);
+          wh[u] = pack_half2(kh2.x, kh2.y);
         }
-        *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(ch, j8, 128)) =
-            make_uint4(wk[0], wk[1], wk[2], wk[3]);
-        *reinterpret_cast<uint4*>(sm + kPrepVt + sw128_chunk(ch, j8, 128)) =
-            make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        ktl[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+        *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(kC + r, c16, 128)) =
+            make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
+            make_uint4(wh[0], wh[1], wh[2], wh[3]);
       }
+      if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(Gl[tid]);
+    }
+    __syncthreads();  // every read of the q and k rows is done: their space takes K~ and V
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15;
+      *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = ktl[m];
+      const uint32_t* vb = reinterpret_cast<const uint32_t*>(&vreg[m]);
+      uint32_t wv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        wv[u] = pack_half2(__uint_as_float(vb[u] << 16), __uint_as_float(vb[u] & 0xFFFF0000u));
+      *reinterpret_cast<uint4*>(sm + kPrepV + sw128_chunk(r, c16, kC)) =
+          make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
+
+    // ---- 7. U~^T = V^T T^T (A = V MN-major, B = T) and W = [T; T] K~ (B = K~
+    //      MN-major) on the tensor cores, then both straight to the workspace ----
     if (tid == 0) {
       fence_after_sync();
-      const uint64_t dT = desc_k_sw128(smem_u32(sm + kPrepT), 0);
-      const uint64_t dKt = desc_k_sw128(smem_u32(sm + kPrepKt), 0);
-      const uint64_t dVt = desc_k_sw128(smem_u32(sm + kPrepVt), 0);
+      const uint32_t sT = smem_u32(sm + kPrepTT), sV = smem_u32(sm + kPrepV);
+      const uint32_t sKt = smem_u32(sm + kPrepKt);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tmem, dKt + 2 * ks, dT + 2 * ks, kIdF16N64, ks > 0);
-        mma_ss(tmem + 64, dVt + 2 * ks, dT + 2 * ks, kIdF16N64, ks > 0);
+        mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sT, 32 * ks),
+               kIdUt, ks > 0);
+        mma_ss(tmem + kTdW, desc_k_sw128(sT, 32 * ks), desc_mn_sw128(sKt, ks, kC * 128),
+               kIdW, ks > 0);
       }
       mma_commit(&bar_mma);
-    }
-    // while the MMAs run: -Q~ [t][d_k], K^^T [d_k][t] and G_C straight to the workspace
-    for (int e = tid; e < kC * 16; e += kPrepThreads) {
-      const int c8l = e & 7, tr = (e >> 3) & 63, kb = e >> 9;
-      const int ch = 64 * kb + 8 * c8l;
-      float g8[8], qf[8];
-      ld8f(G + tr * kD + ch, g8);
-      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + tr * 256 + ch * 2), qf);
-      const float iq = -s_invq[tr];
-      uint32_t w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        w[u] = pack_half2(qf[2 * u] * iq * ex2f(g8[2 * u]), qf[2 * u + 1] * iq * ex2f(g8[2 * u + 1]));
-      *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(64 + tr, 8 * kb + c8l, 128)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    {
-      const int ch = tid & (kD - 1), tq = tid >> 7;
-      const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(sm + kPrepK);
-      const float gl = G[(kC - 1) * kD + ch];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int t8 = 4 * tq + m;
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int r0 = 8 * t8 + 2 * u;
-          w[u] = pack_half2(
-              __bfloat162float(kr[r0 * kD + ch]) * s_invk[r0] * ex2f(gl - G[r0 * kD + ch]),
-              __bfloat162float(kr[(r0 + 1) * kD + ch]) * s_invk[r0 + 1] *
-                  ex2f(gl - G[(r0 + 1) * kD + ch]));
-        }
-        *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(ch, t8, 128)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      if (tq == 0) reinterpret_cast<float*>(ws + kWsGam)[ch] = ex2f(gl);
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
     mma_phase ^= 1;
     if (!ok) goto fail;
     fence_after_sync();
-
-    // ---- 7. W (B [t][d_k]) via a shared-memory transpose; U~^T (A [d_v][t]) direct ----
     {
+      // warp (quarter, chalf): U~^T rows ch = its TMEM lanes, columns t = 32 chalf ..;
+      // W rows t = its lanes mod 64 (both copies), 32-column slab 2 chalf + quarter / 2
       const int quarter = warp & 3, chalf = warp >> 2;
-      const int ch = quarter * 32 + lane;
+      const int lrow = quarter * 32 + lane, slab = 2 * chalf + (quarter >> 1);
       uint32_t x[32], y[32];
-      tmem_ld32(taddr(tmem, quarter * 32, 64 + 32 * chalf), x);  // U~^T[ch][t]
-      tmem_ld32(taddr(tmem, quarter * 32, 32 * chalf), y);       // W^T[ch][t]
-      tmem_wait_ld();  // t = 32 chalf + j
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        *reinterpret_cast<__half*>(sm + kPrepWst + sw128_offset(32 * chalf + j, ch, 128)) =
-            __float2half_rn(__uint_as_float(y[j]));
+      tmem_ld32(taddr(tmem, quarter * 32, kTdU + 32 * chalf), x);
+      tmem_ld32(taddr(tmem, quarter * 32, kTdW + 32 * slab), y);
+      tmem_wait_ld();
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
         uint32_t w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           w[u] = pack_half2(__uint_as_float(x[8 * c8 + 2 * u]), __uint_as_float(x[8 * c8 + 2 * u + 1]));
-        *reinterpret_cast<uint4*>(ws + kWsUt + sw128_chunk(ch, 4 * chalf + c8, 128)) =
+        *reinterpret_cast<uint4*>(ws + kWsUt + sw128_chunk(lrow, 4 * chalf + c8, 128)) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
-    }
-    __syncthreads();
-    for (int e = tid; e < 1024; e += kPrepThreads) {  // rows 0..63 of both K-blocks
-      const int u = e < 512 ? e : e + 512;
-      reinterpret_cast<uint4*>(ws + kWsWQ)[u] = reinterpret_cast<const uint4*>(sm + kPrepWst)[u];
+      const int tw = lrow & (kC - 1);
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          w[u] = pack_half2(__uint_as_float(y[8 * c8 + 2 * u]), __uint_as_float(y[8 * c8 + 2 * u + 1]));
+        *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(tw, 4 * slab + c8, 128)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
     }
   }
   goto done;
@@ -642,7 +640,7 @@ done:
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tmem, 128);
+  if (warp == 0) tmem_dealloc(tmem, kPrepTmemCols);
 }
 
 // ============================================================ chain kernel
@@ -841,10 +839,11 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       if (tid == 0) {
         fence_after_sync();
         const uint32_t sb = smem_u32(buf);
-        const uint64_t dKh = desc_k_sw128(sb + kWsKh, 0), dP = desc_k_sw128(sb + kWsP, 0);
+        const uint64_t dP = desc_k_sw128(sb + kWsP, 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // S^T += U^T K^: the state chain first
-          mma_ts(tmem + kTS, tmem + tAU + 8 * ks, dKh + 2 * ks, kIdF16N128, 1);
+          mma_ts(tmem + kTS, tmem + tAU + 8 * ks, desc_mn_sw128(sb + kWsKh, ks, kC * 128),
+                 kIdKh, 1);
         mma_commit(&bar_s);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // O^T += U^T P^T

@@ -55,11 +55,25 @@ __host__ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t 
   return sw128_offset(row, c8 * 8u, rows);
 }
 
+// MN-major operand in the 128-byte-swizzled canonical layout: the operand's
+// K index runs over 128-byte rows holding 64 consecutive M (or N) elements,
+// 8-row K groups are 1024 B apart (SBO), and 64-element M/N blocks are
+// `mn_block_bytes` apart (LBO).  A K-step of 16 starts 2048 B further on.
+// Storage is that of the K-major SW128 tile of the transpose: element (mn, k)
+// of an operand with K extent `kext` sits at sw128_offset(k, mn, kext).
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t tile_saddr, uint32_t kstep,
+                                                  uint32_t mn_block_bytes) {
+  return smem_desc(tile_saddr + kstep * 2048u, mn_block_bytes, 1024u, kSwizzle128B);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulation:
 // D format F32 (bits 4-5 = 1), A/B format at bits 7-9 / 10-12 (0 = F16,
-// 1 = BF16), both operands K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16) {
+// 1 = BF16), A/B major-ness at bits 15 / 16 (0 = K-major, 1 = MN-major),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool a_mn = false,
+                                                 bool b_mn = false) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 

@@ -1,8 +1,9 @@
 // umma_selftest.cu -- checks of the tensor-core building blocks in
 // linear_attention_recurrence_prefill_gb300/csrc/umma.cuh, driven by
 // tests/test_umma.py: one tcgen05.mma chain (A from shared memory or from TMEM,
-// B from shared memory, both in the 128-byte-swizzled K-major layout), TMEM
-// load/store, mbarrier waits with a bound, and 1-D bulk copies.
+// B from shared memory; each shared-memory operand in the 128-byte-swizzled
+// K-major or MN-major layout), TMEM load/store, mbarrier waits with a bound,
+// and 1-D bulk copies.
 //
 // Every wait is bounded; on a timeout the kernel records it and returns.
 #include <cuda_runtime.h>
@@ -19,10 +20,13 @@ constexpr long long kLimit = 2000000000LL;  // ~1 s of cycles
 // D[128 x N] = A[128 x K] * B[N x K]^T, fp32 accumulate.
 // A, B: row-major 16-bit (fp16 or bf16) in global memory.  a_in_tmem: A is
 // staged in TMEM (fp16/bf16 pairs per 32-bit column) instead of shared memory.
+// a_mn / b_mn: that operand is staged MN-major (64-element M/N blocks of
+// K rows of 128 B) instead of K-major.
 __global__ void __launch_bounds__(128) mma_kernel(const uint16_t* __restrict__ A,
                                                   const uint16_t* __restrict__ B,
                                                   float* __restrict__ D, int N, int K,
-                                                  uint32_t idesc, int a_in_tmem, int* status) {
+                                                  uint32_t idesc, int a_in_tmem, int a_mn,
+                                                  int b_mn, int* status) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar;
   __shared__ uint32_t tmem_base;
@@ -32,14 +36,16 @@ __global__ void __launch_bounds__(128) mma_kernel(const uint16_t* __restrict__ A
   uint8_t* sB = sA + 128 * K * 2;
   const int tid = threadIdx.x, warp = tid >> 5;
 
-  // operands into the swizzled K-major layout
+  // operands into the swizzled K-major or MN-major layout
   for (int e = tid; e < 128 * K; e += 128) {
     const int r = e / K, k = e % K;
-    *reinterpret_cast<uint16_t*>(sA + sw128_offset(r, k, 128)) = A[e];
+    const uint32_t off = a_mn ? sw128_offset(k, r, K) : sw128_offset(r, k, 128);
+    *reinterpret_cast<uint16_t*>(sA + off) = A[e];
   }
   for (int e = tid; e < N * K; e += 128) {
     const int r = e / K, k = e % K;
-    *reinterpret_cast<uint16_t*>(sB + sw128_offset(r, k, N)) = B[e];
+    const uint32_t off = b_mn ? sw128_offset(k, r, K) : sw128_offset(r, k, N);
+    *reinterpret_cast<uint16_t*>(sB + off) = B[e];
   }
   if (tid == 0) {
     mbar_init(&bar, 1);
@@ -78,11 +84,13 @@ __global__ void __launch_bounds__(128) mma_kernel(const uint16_t* __restrict__ A
   if (tid == 0) {
     for (int ks = 0; ks < K / 16; ++ks) {
       const uint32_t kb = ks >> 2, kbyte = (ks & 3) * 32;
-      const uint64_t bdesc = desc_k_sw128(smem_u32(sB) + kb * N * 128, kbyte);
+      const uint64_t bdesc = b_mn ? desc_mn_sw128(smem_u32(sB), ks, K * 128)
+                                  : desc_k_sw128(smem_u32(sB) + kb * N * 128, kbyte);
       if (a_in_tmem) {
         mma_ts(d_tmem, a_tmem + ks * 8, bdesc, idesc, ks > 0);
       } else {
-        const uint64_t adesc = desc_k_sw128(smem_u32(sA) + kb * 128 * 128, kbyte);
+        const uint64_t adesc = a_mn ? desc_mn_sw128(smem_u32(sA), ks, K * 128)
+                                    : desc_k_sw128(smem_u32(sA) + kb * 128 * 128, kbyte);
         mma_ss(d_tmem, adesc, bdesc, idesc, ks > 0);
       }
     }
@@ -143,16 +151,19 @@ extern "C" {
 
 // Returns 0 on success, 1 if the kernel reported a timeout, -1 on a CUDA error.
 int selftest_mma(const void* A, const void* B, float* D, int N, int K, int bf16,
-                 int a_in_tmem) {
+                 int a_in_tmem, int a_mn, int b_mn) {
   if (N % 16 || N < 16 || N > 128 || K % 64 || K < 64 || K > 128) return -2;
+  if ((a_mn && a_in_tmem) || (b_mn && N % 64)) return -2;  // MN-major: whole 64-wide blocks
   int* status = nullptr;
   if (cudaMalloc(&status, sizeof(int)) != cudaSuccess) return -1;
   cudaMemset(status, 0, sizeof(int));
-  const size_t smem = 1024 + (size_t)(128 + N) * K * 2;
+  // 64 KB of slack past the operands: any descriptor reads stay inside the allocation
+  const size_t smem = 1024 + (size_t)(128 + N) * K * 2 + 65536;
   cudaFuncSetAttribute(mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   mma_kernel<<<1, 128, smem>>>(static_cast<const uint16_t*>(A),
                                static_cast<const uint16_t*>(B), D, N, K,
-                               idesc_f16(128, N, bf16 != 0), a_in_tmem, status);
+                               idesc_f16(128, N, bf16 != 0, a_mn != 0, b_mn != 0), a_in_tmem,
+                               a_mn, b_mn, status);
   cudaError_t e = cudaDeviceSynchronize();
   int h = 0;
   cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost);

@@ -28,7 +28,7 @@ def lib():
         subprocess.run(cmd, check=True)
     l = ctypes.CDLL(OUT)
     vp, ci = ctypes.c_void_p, ctypes.c_int
-    l.selftest_mma.argtypes = [vp, vp, vp, ci, ci, ci, ci]
+    l.selftest_mma.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, ci]
     l.selftest_mma.restype = ci
     l.selftest_bulk.argtypes = [vp, vp, ctypes.POINTER(ci), ci]
     l.selftest_bulk.restype = ci
@@ -44,7 +44,22 @@ def test_mma(lib, a_in_tmem, dtype, N, K):
     B = torch.randn((N, K), generator=g, device="cuda").to(dtype)
     D = torch.full((128, N), float("nan"), device="cuda")
     rc = lib.selftest_mma(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K,
-                          int(dtype == torch.bfloat16), a_in_tmem)
+                          int(dtype == torch.bfloat16), a_in_tmem, 0, 0)
+    assert rc == 0, f"selftest_mma returned {rc}"
+    ref = A.double() @ B.double().T
+    err = (D.double() - ref).abs().max().item()
+    assert err < 1e-3 * max(1.0, ref.abs().max().item()), f"max abs error {err}"
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(1, 0), (0, 1), (1, 1)], ids=["A_mn", "B_mn", "AB_mn"])
+@pytest.mark.parametrize("N,K", [(64, 64), (128, 64), (128, 128), (64, 128)])
+def test_mma_mn_major(lib, a_mn, b_mn, N, K):
+    """MN-major operands (the layout the prefill uses for V, K~ and K^)."""
+    g = torch.Generator(device="cuda").manual_seed(7 * N + K + 10 * a_mn + 20 * b_mn)
+    A = torch.randn((128, K), generator=g, device="cuda").half()
+    B = torch.randn((N, K), generator=g, device="cuda").half()
+    D = torch.full((128, N), float("nan"), device="cuda")
+    rc = lib.selftest_mma(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, 0, 0, a_mn, b_mn)
     assert rc == 0, f"selftest_mma returned {rc}"
     ref = A.double() @ B.double().T
     err = (D.double() - ref).abs().max().item()
