@@ -163,8 +163,11 @@ constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
 //   Gram (per 64-channel half): A hi/lo [128 x 64] bf16 SW128, B hi/lo [16 x 64]
 constexpr uint32_t kPrepAhi = kPrepX, kPrepAlo = kPrepX + 16384;
 constexpr uint32_t kPrepBhi = kPrepX + 32768, kPrepBlo = kPrepX + 34816;
-//   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64], scratch
-constexpr uint32_t kPrepAmat = kPrepX, kPrepInv = kPrepX + 16384, kPrepY = kPrepX + 32768;
+//   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64] with padded row
+//   strides (no bank conflicts between the rows a warp touches), 3 KB scratch
+constexpr int kAs = 66, kXs = 68;  // row strides (floats) of A and of the inverse
+constexpr uint32_t kPrepAmat = kPrepX, kPrepInv = kPrepX + kC * kAs * 4;
+constexpr uint32_t kPrepY = kPrepInv + kC * kXs * 4;
 //   W / U~ MMAs: [T; T] [128 (t) x 64 (j)] fp16 K-major over A; V and K~ [64 (j) rows
 //   of 128 channels] fp16 MN-major over the q and k rows
 constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
@@ -174,6 +177,11 @@ constexpr uint32_t kIdUt = idesc_f16(128, 64, false, true, false);  // A MN-majo
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
+static_assert(kPrepY + 3 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
+static_assert(kPrepBlo + 2048 <= kPrepSmall, "Gram operands inside the reused region");
+static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
+static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
+              "float4 access to the inverse and the scratch");
 
 __device__ __forceinline__ float ex2f(float x) {  // hardware 2^x (rel. error ~2^-22)
   float y;
@@ -309,23 +317,43 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   bool ok = true;
   __syncthreads();
 
-  // ---- 2. running log2-decay per channel; L2 norms of the q, k rows ----
+  // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
+  //      registers); L2 norms of the q, k rows (warps 4-7, four rows at a time) ----
   if (tid < kD) {
+    float x[kC];
+#pragma unroll
+    for (int r = 0; r < kC; ++r) x[r] = G[r * kD + tid];
     float run = 0.f;
+#pragma unroll
     for (int r = 0; r < kC; ++r) {
-      run += fminf(fmaxf(G[r * kD + tid], a.g_min), 0.f) * kLog2e;
-      G[r * kD + tid] = run;
+      run += fminf(fmaxf(x[r], a.g_min), 0.f) * kLog2e;
+      x[r] = run;
     }
+#pragma unroll
+    for (int r = 0; r < kC; ++r) G[r * kD + tid] = x[r];
   } else {
-    for (int rr = warp - 4; rr < 2 * kC; rr += 4) {
-      const int r = rr & (kC - 1);
-      const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
-      const uint2 x = *reinterpret_cast<const uint2*>(src + lane * 8);
-      const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
-      const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
-      const float ss = warp_sum(x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y) + a.eps_l2;
-      if (lane == 0) {
-        const float inv = a.l2norm_qk ? (ss > 0.f ? 1.0f / sqrtf(ss) : 0.f) : 1.f;
+#pragma unroll 1
+    for (int i0 = 0; i0 < 32; i0 += 4) {  // rows rr = (warp - 4) + 4 i, i = i0 .. i0 + 3
+      float ss[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int rr = (warp - 4) + 4 * (i0 + u), r = rr & (kC - 1);
+        const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
+        const uint2 x = *reinterpret_cast<const uint2*>(src + lane * 8);
+        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+        ss[u] = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+      }
+      if (lane < 4) {  // lane u finishes row u of the group
+        const float sl = (lane == 0 ? ss[0] : lane == 1 ? ss[1] : lane == 2 ? ss[2] : ss[3]) +
+                         a.eps_l2;
+        const int rr = (warp - 4) + 4 * (i0 + lane), r = rr & (kC - 1);
+        const float inv = a.l2norm_qk ? (sl > 0.f ? rsqrtf(sl) : 0.f) : 1.f;
         if (rr < kC) s_invq[r] = inv * a.q_scale;
         else s_invk[r] = inv;
       }
@@ -335,14 +363,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 
   // ---- 3. Gram matrices: column tile b, 64-channel half kh at a time ----
   //   A rows r >= 16b: [k^_r ; q^_r] * 2^(g_r - gend_b);  B rows j in tile b:
-  //   k^_j * 2^(gend_b - g_j); bf16 hi/lo; D[:, 16b..16b+15] += A B^T (3 products)
+  //   k^_j * 2^(gend_b - g_j); bf16 hi/lo; D[:, 16b..16b+15] += A B^T (3 products).
+  //   Pipelined: a round's operand items are computed into registers while the
+  //   previous round's MMAs still read the operand tiles, then stored.
 #pragma unroll 1
   for (int round = 0; round < 8; ++round) {
     const int b = round >> 1, kh = round & 1;
-    const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group)
+    const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group), then 128 B items
     const float* gend = G + (16 * b + 15) * kD + 64 * kh;
-    for (int it = tid; it < nA + 128; it += kPrepThreads) {
-      if (it < nA) {
+    uint4 iv0[3], iv1[3], iv2[3], iv3[3];
+    uint32_t io0[3], io1[3];
+    int kind[3];  // 0: none, 1: A item, 2: B item
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+      const int it = tid + kPrepThreads * s;
+      kind[s] = it < nA ? 1 : (it < nA + 128 ? 2 : 0);
+      if (kind[s] == 1) {
         const int r = 16 * b + (it >> 3), c8 = it & 7;
         const int ch = 64 * kh + 8 * c8;
         float g8[8], ge[8], kf[8], qf[8];
@@ -361,12 +397,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]), mul2(e, ik2)), khi[u], klo[u]);
           split2v(mul2(make_float2(qf[2 * u], qf[2 * u + 1]), mul2(e, iq2)), qhi[u], qlo[u]);
         }
-        const uint32_t ok_ = sw128_chunk(r, c8, 128), oq = sw128_chunk(64 + r, c8, 128);
-        *reinterpret_cast<uint4*>(sm + kPrepAhi + ok_) = make_uint4(khi[0], khi[1], khi[2], khi[3]);
-        *reinterpret_cast<uint4*>(sm + kPrepAlo + ok_) = make_uint4(klo[0], klo[1], klo[2], klo[3]);
-        *reinterpret_cast<uint4*>(sm + kPrepAhi + oq) = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
-        *reinterpret_cast<uint4*>(sm + kPrepAlo + oq) = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
-      } else {
+        iv0[s] = make_uint4(khi[0], khi[1], khi[2], khi[3]);
+        iv1[s] = make_uint4(klo[0], klo[1], klo[2], klo[3]);
+        iv2[s] = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
+        iv3[s] = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
+        io0[s] = sw128_chunk(r, c8, 128);
+        io1[s] = sw128_chunk(64 + r, c8, 128);
+      } else if (kind[s] == 2) {
         const int e = it - nA, jj = e >> 3, c8 = e & 7;
         const int j = 16 * b + jj, ch = 64 * kh + 8 * c8;
         float g8[8], ge[8], kf[8];
@@ -383,14 +420,33 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]),
                        mul2(make_float2(ex2f(d.x), ex2f(d.y)), ik2)), hi[u], lo[u]);
         }
-        const uint32_t o = sw128_chunk(jj, c8, 16);
-        *reinterpret_cast<uint4*>(sm + kPrepBhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sm + kPrepBlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        iv0[s] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        iv1[s] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        io0[s] = sw128_chunk(jj, c8, 16);
+      }
+    }
+    bool waited = true;
+    if (round > 0) {  // the previous round's MMAs must be done reading the tiles
+      waited = mbar_wait(&bar_mma, mma_phase, t.spins);
+      mma_phase ^= 1;
+      fence_after_sync();
+    }
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+      if (kind[s] == 1) {
+        *reinterpret_cast<uint4*>(sm + kPrepAhi + io0[s]) = iv0[s];
+        *reinterpret_cast<uint4*>(sm + kPrepAlo + io0[s]) = iv1[s];
+        *reinterpret_cast<uint4*>(sm + kPrepAhi + io1[s]) = iv2[s];
+        *reinterpret_cast<uint4*>(sm + kPrepAlo + io1[s]) = iv3[s];
+      } else if (kind[s] == 2) {
+        *reinterpret_cast<uint4*>(sm + kPrepBhi + io0[s]) = iv0[s];
+        *reinterpret_cast<uint4*>(sm + kPrepBlo + io0[s]) = iv1[s];
       }
     }
     fence_proxy_async();
     fence_before_sync();
-    __syncthreads();
+    ok = __syncthreads_and(waited);
+    if (!ok) goto fail;
     if (tid == 0) {
       fence_after_sync();
       const uint32_t d = tmem + 16 * b;
@@ -408,11 +464,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       for (int ks = 0; ks < 4; ++ks) mma_ss(d, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, 1u);
       mma_commit(&bar_mma);
     }
-    ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
-    mma_phase ^= 1;
-    if (!ok) goto fail;
-    fence_after_sync();
   }
+  ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
+  mma_phase ^= 1;
+  if (!ok) goto fail;
+  fence_after_sync();
 
   {
     // ---- 4. A (lanes 0..63) to shared memory, P (lanes 64..127) to the workspace ----
@@ -428,7 +484,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int jj = 32 * chalf + j;
-          Amat[r * kC + jj] = (jj < r) ? br * __uint_as_float(x[j]) : 0.f;
+          Amat[r * kAs + jj] = (jj < r) ? br * __uint_as_float(x[j]) : 0.f;
         }
       } else {
         const int tr = r - kC;
@@ -463,7 +519,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     // ---- 5. X = (I + A)^-1 by 16 x 16 blocks ----
     float* X = reinterpret_cast<float*>(sm + kPrepInv);
     float* Y = reinterpret_cast<float*>(sm + kPrepY);
-    for (int e = tid; e < kC * kC; e += kPrepThreads) X[e] = 0.f;
+    for (int e = tid; e < kC * kXs; e += kPrepThreads) X[e] = 0.f;
     __syncthreads();
     if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc)
       const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;
@@ -472,11 +528,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       for (int r = 0; r < 16; ++r) {
         float acc = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-        for (int m = 0; m < r; ++m) acc -= Amat[(o + r) * kC + o + m] * x[m];
+        for (int m = 0; m < r; ++m) acc -= Amat[(o + r) * kAs + o + m] * x[m];
         x[r] = acc;
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) X[(o + r) * kC + o + cc] = x[r];
+      for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
     }
     __syncthreads();
     // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj;
@@ -486,10 +542,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       for (int e = tid; e < nblk * 64; e += kPrepThreads) {
         const int bj = e >> 6, bi = bj + dd, r = (e >> 2) & 15, c4 = (e & 3) * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* arow = Amat + (16 * bi + r) * kC;
+        const float* arow = Amat + (16 * bi + r) * kAs;
         for (int m = 16 * bj; m < 16 * bi; ++m) {
           const float am = arow[m];
-          const float4 x4 = *reinterpret_cast<const float4*>(X + m * kC + 16 * bj + c4);
+          const float4 x4 = *reinterpret_cast<const float4*>(X + m * kXs + 16 * bj + c4);
           acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
         }
         *reinterpret_cast<float4*>(Y + (bj << 8) + r * 16 + c4) = acc;
@@ -498,14 +554,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       for (int e = tid; e < nblk * 64; e += kPrepThreads) {
         const int bj = e >> 6, bi = bj + dd, r = (e >> 2) & 15, c4 = (e & 3) * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* xrow = X + (16 * bi + r) * kC + 16 * bi;
+        const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
           const float xm = xrow[m];
           const float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
           acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
         }
-        *reinterpret_cast<float4*>(X + (16 * bi + r) * kC + 16 * bj + c4) =
+        *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
       __syncthreads();
@@ -520,7 +576,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j0 = 8 * c8 + 2 * u;
-        w[u] = pack_half2(X[tr * kC + j0] * s_beta[j0], X[tr * kC + j0 + 1] * s_beta[j0 + 1]);
+        const float2 x2 = *reinterpret_cast<const float2*>(X + tr * kXs + j0);
+        w[u] = pack_half2(x2.x * s_beta[j0], x2.y * s_beta[j0 + 1]);
       }
       const uint4 wt = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(tr, c8, 128)) = wt;
