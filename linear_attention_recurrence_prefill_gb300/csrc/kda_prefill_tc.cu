@@ -702,9 +702,11 @@ done:
 
 // ============================================================ chain kernel
 // 384 threads.  Warps 0-7 carry the state (conversions split by column half,
-// thread 0 also issues the MMAs and the bulk loads); warps 8-11 run the
-// epilogue from a double-buffered O^T, overlapping the next chunk.  Warp w
-// touches TMEM lanes 32*(w%4) .. +31 (lane = d_v index).  Per chunk i:
+// thread 0 also issues the state chain's MMAs); warps 8-11 run the epilogue
+// from a double-buffered O^T, overlapping the next chunk, and their first
+// thread issues the bulk loads and the state-free first product of each chunk
+// two chunks ahead.  Warp w touches TMEM lanes 32*(w%4) .. +31 (lane = d_v
+// index).  Per chunk i:
 //   [U^T | O^T] = U~^T [I | 0]                  (4 MMAs, N = 128, no state needed)
 //   -S^T -> fp16 operand, S^T <- S^T Diag(G_C)   (state warps)
 //   [U^T | O^T] += (-S^T) [W ; -Q~]^T           (8 MMAs, N = 128)
@@ -726,16 +728,19 @@ constexpr uint32_t kChSmem = kChE + kC * kEStride * 4 + 1024;
 // U^T fp16 operand in two buffers
 constexpr uint32_t kTS = 0, kTUO0 = 128, kTAS = 384, kTAU0 = 448;
 constexpr uint32_t kBarState = 1, kBarEpi = 2;  // named barriers of the two groups
+constexpr int kIssuer = kChState;  // epilogue thread that issues the loads and init MMAs
 
-// sigmoid with the hardware exp2 / reciprocal approximations (relative error
-// a few 1e-7, far below the bf16 output rounding)
-__device__ __forceinline__ float fast_sigmoid(float x) {
-  return __fdividef(1.0f, 1.0f + __expf(-x));
+// Hardware tanh (tanh.approx.f32, maximum relative error about 2^-11); the
+// gate uses sigmoid(x) = (1 + tanh(x / 2)) / 2, one MUFU operation per value.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_u, bar_s, bar_o[2], bar_oe[2], bar_dbg;
+  __shared__ uint64_t bar_full[2], bar_init[2], bar_u, bar_s, bar_o[2], bar_dbg, bar_drain;
   __shared__ uint32_t tmem_base;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -759,9 +764,10 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     mbar_init(&bar_s, 1);
     mbar_init(&bar_o[0], 1);
     mbar_init(&bar_o[1], 1);
-    mbar_init(&bar_oe[0], 4);  // one arrival per epilogue warp
-    mbar_init(&bar_oe[1], 4);
+    mbar_init(&bar_init[0], 1);
+    mbar_init(&bar_init[1], 1);
     mbar_init(&bar_dbg, 1);
+    mbar_init(&bar_drain, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -782,6 +788,9 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     *reinterpret_cast<uint4*>(sm + kChId + sw128_chunk(r, c8, 128)) =
         make_uint4(w[0], w[1], w[2], w[3]);
   }
+  fence_proxy_async();  // the MMAs read the [I; 0] tile
+  // The bulk loads of the chunk blocks and the [U^T | O^T] = U~^T [I | 0] MMAs
+  // are issued by one epilogue thread (kIssuer), off the state chain.
   auto issue_load = [&](int i) {
     uint8_t* dst = sm + ((i & 1) ? kChBuf1 : kChBuf0);
     const uint8_t* src = ws_block(t, cbase + i, h);
@@ -789,8 +798,8 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     for (int p = 0; p < kWsParts; ++p)
       bulk_g2s(dst + kWsPartOff[p], src + kWsPartOff[p], kWsPartLen[p], &bar_full[i & 1]);
   };
-  int issued = 0;  // loads issued (thread 0)
-  if (tid == 0) {
+  int issued = 0, landed = 0;  // kIssuer: loads issued / loads seen complete
+  if (tid == kIssuer) {
     for (int i = 0; i < 2 && i < nchunks; ++i) issue_load(i);
     issued = min(2, nchunks);
   }
@@ -813,30 +822,14 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       tmem_st32(lane_base + kTS + c0, r);
     }
     tmem_wait_st();
-    int consumed = 0;
     for (int i = 0; i < nchunks; ++i) {
       const uint8_t* buf = sm + ((i & 1) ? kChBuf1 : kChBuf0);
       const uint32_t tUO = tmem + kTUO0 + 128 * (i & 1), tAU = kTAU0 + 32 * (i & 1);
       bool w = mbar_wait(&bar_full[i & 1], (i >> 1) & 1, t.spins);
       if (i > 0) w = w && mbar_wait(&bar_s, (i - 1) & 1, t.spins);
-      if (tid == 0 && i > 0) w = w && mbar_wait(&bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1, t.spins);
-      if (tid == 0 && i >= 2) w = w && mbar_wait(&bar_oe[i & 1], ((i - 2) >> 1) & 1, t.spins);
       ok = named_sync_and(kBarState, kChState, w);
       if (!ok) break;
-      consumed = i + 1;
       fence_after_sync();
-      if (tid == 0) {
-        if (i >= 1 && i + 1 < nchunks) {  // every MMA of chunk i-1 is done: reuse its buffer
-          fence_proxy_async();
-          issue_load(i + 1);
-          issued = i + 2;
-        }
-        // [U^T | O^T] = U~^T [I | 0]: independent of the state, start it now
-        const uint64_t dUt = desc_k_sw128(smem_u32(buf) + kWsUt, 0);
-        const uint64_t dId = desc_k_sw128(smem_u32(sm + kChId), 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) mma_ss(tUO, dUt + 2 * ks, dId + 2 * ks, kIdF16N128, ks > 0);
-      }
       // -S^T (fp16) into the A operand, S^T Diag(G_C) back into the accumulator
       {
         const float4* gam4 = reinterpret_cast<const float4*>(buf + kWsGam) + 16 * chalf;
@@ -868,17 +861,23 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       }
       fence_before_sync();
       named_sync(kBarState, kChState);
+      bool winit = true;
       if (tid == 0) {
+        fence_after_sync();
+        // [U^T | O^T] = U~^T [I | 0] must be in place (issued by kIssuer)
+        winit = mbar_wait(&bar_init[i & 1], (i >> 1) & 1, t.spins);
         fence_after_sync();
         const uint64_t dWQ = desc_k_sw128(smem_u32(buf) + kWsWQ, 0);
         // [U^T | O^T] += (-S^T) [W ; -Q~]^T.  K-step: +2 in the descriptor's
         // address field (32 bytes); K-block of 64: +1024 (16 KB)
+        if (winit) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N128, 1);
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N128, 1);
+        }
         mma_commit(&bar_u);
       }
-      ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_u, i & 1, t.spins));
+      ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_u, i & 1, t.spins) && winit);
       if (!ok) break;
       fence_after_sync();
       {  // U^T -> fp16 A operand (column half per warp)
@@ -927,7 +926,6 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       report(a.status, KDA_ERR_TIMEOUT);
       mma_commit(&bar_dbg);
       mbar_wait(&bar_dbg, 0, t.spins);
-      for (int j = consumed; j < issued; ++j) mbar_wait(&bar_full[j & 1], (j >> 1) & 1, t.spins);
     }
   } else {
     // ---------------- epilogue warps: O^T (lane = d_v) -> E[t][d_v] -> rows of y.
@@ -937,6 +935,26 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     const __nv_bfloat16* gate = static_cast<const __nv_bfloat16*>(a.gate);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
     float* E = reinterpret_cast<float*>(sm + kChE);
+    // kIssuer: [U^T | O^T](i) = U~^T [I | 0] once chunk i's block has landed
+    auto issue_init = [&](int i) {
+      const uint8_t* buf = sm + ((i & 1) ? kChBuf1 : kChBuf0);
+      const uint32_t tUO = tmem + kTUO0 + 128 * (i & 1);
+      const uint64_t dUt = desc_k_sw128(smem_u32(buf) + kWsUt, 0);
+      const uint64_t dId = desc_k_sw128(smem_u32(sm + kChId), 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) mma_ss(tUO, dUt + 2 * ks, dId + 2 * ks, kIdF16N128, ks > 0);
+      mma_commit(&bar_init[i & 1]);
+    };
+    bool iss_ok = true;
+    if (tid == kIssuer) {
+      for (int i = 0; i < 2 && i < nchunks && iss_ok; ++i) {
+        iss_ok = mbar_wait(&bar_full[i & 1], (i >> 1) & 1, t.spins);
+        if (iss_ok) {
+          landed = i + 1;
+          issue_init(i);
+        }
+      }
+    }
     for (int i = 0; i < nchunks; ++i) {
       const int tok0 = s0 + i * kC;
       const int len = min(kC, s1 - tok0);
@@ -947,12 +965,18 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) graw[c] = *reinterpret_cast<const uint4*>(gate + gofs + 8 * c);
       }
-      ok = named_sync_and(kBarEpi, 128, mbar_wait(&bar_o[i & 1], (i >> 1) & 1, t.spins));
+      ok = named_sync_and(kBarEpi, 128,
+                          mbar_wait(&bar_o[i & 1], (i >> 1) & 1, t.spins) && iss_ok);
       if (!ok) {
         if (et == 0) report(a.status, KDA_ERR_TIMEOUT);
         break;
       }
       fence_after_sync();
+      if (tid == kIssuer && i + 2 < nchunks) {  // every MMA of chunk i is done: its
+        fence_proxy_async();                    // buffer takes chunk i + 2
+        issue_load(i + 2);
+        issued = i + 3;
+      }
       {
         uint32_t x0[32], x1[32];
         const uint32_t tO = lane_base + kTUO0 + 128 * (i & 1) + 64;
@@ -966,8 +990,7 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
         }
       }
       fence_before_sync();
-      named_sync(kBarEpi, 128);
-      if (lane == 0) mbar_arrive(&bar_oe[i & 1]);  // the [U|O] buffer may be overwritten
+      named_sync(kBarEpi, 128);  // O^T(i) is out of TMEM: the [U|O] buffer may be reused
       // pass 1: sum of squares of the row; pass 2: outputs, 8 channels at a time
       const float4* er4 = reinterpret_cast<const float4*>(&E[er * kEStride + 64 * eh]);
       float ss = 0.f;
@@ -978,6 +1001,7 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       const float inv = gate ? rsqrtf(ss * (1.0f / kD) + a.eps_norm) : 1.f;
+      const float hinv = 0.5f * inv;  // inv * sigmoid(g) = hinv * tanh(g / 2) + hinv
       if (live) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -988,8 +1012,8 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const float2 gf = __bfloat1622float2(g2[u]);
-              y[2 * u] *= inv * fast_sigmoid(gf.x);
-              y[2 * u + 1] *= inv * fast_sigmoid(gf.y);
+              y[2 * u] *= fmaf(tanh_approx(0.5f * gf.x), hinv, hinv);
+              y[2 * u + 1] *= fmaf(tanh_approx(0.5f * gf.y), hinv, hinv);
             }
             if (a.norm_weight) {
               const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 64 * eh + 8 * c);
@@ -1006,7 +1030,23 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
           *reinterpret_cast<uint4*>(o + gofs + 8 * c) = out;
         }
       }
+      if (tid == kIssuer && i + 2 < nchunks) {
+        fence_after_sync();
+        iss_ok = mbar_wait(&bar_full[i & 1], ((i + 2) >> 1) & 1, t.spins);
+        if (iss_ok) {
+          landed = i + 3;
+          issue_init(i + 2);
+        }
+      }
       named_sync(kBarEpi, 128);  // E is free again
+    }
+    if (tid == kIssuer && (!ok || !iss_ok)) {
+      // a bounded wait gave up: wait (bounded) for this thread's own MMAs and
+      // bulk copies before TMEM and shared memory are released
+      report(a.status, KDA_ERR_TIMEOUT);
+      mma_commit(&bar_drain);
+      mbar_wait(&bar_drain, 0, t.spins);
+      for (int j = landed; j < issued; ++j) mbar_wait(&bar_full[j & 1], (j >> 1) & 1, t.spins);
     }
   }
   fence_before_sync();
