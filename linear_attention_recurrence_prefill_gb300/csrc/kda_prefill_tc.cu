@@ -701,34 +701,34 @@ done:
 }
 
 // ============================================================ chain kernel
-// 384 threads.  Warps 0-7 carry the state (conversions split by column half,
-// thread 0 also issues the state chain's MMAs); warps 8-11 run the epilogue
-// from a double-buffered O^T, overlapping the next chunk, and their first
-// thread issues the bulk loads and the state-free first product of each chunk
-// two chunks ahead.  Warp w touches TMEM lanes 32*(w%4) .. +31 (lane = d_v
-// index).  Per chunk i:
-//   [U^T | O^T] = U~^T [I | 0]                  (4 MMAs, N = 128, no state needed)
+// 512 threads.  Warps 0-7 carry the state (conversions split by column half;
+// thread 0 also issues the MMAs); warps 8-15 run the epilogue from a
+// double-buffered O^T, overlapping the next chunk, and their first thread
+// issues the bulk load of chunk i + 2 as soon as chunk i's MMAs are done.  Warp w touches TMEM lanes 32*(w%4) .. +31 (lane = d_v index).  Per
+// chunk i:
 //   -S^T -> fp16 operand, S^T <- S^T Diag(G_C)   (state warps)
-//   [U^T | O^T] += (-S^T) [W ; -Q~]^T           (8 MMAs, N = 128)
-//   U^T -> fp16 operand                          (state warps)
+//   [D | O^T] = (-S^T) [W ; -Q~]^T              (8 MMAs, N = 128)
+//   U^T = U~^T + D -> fp16 operand               (state warps, U~^T from the block)
 //   S^T += U^T K^ (the critical path), O^T += U^T P^T
 //   y rows from O^T                              (epilogue warps)
 // Every bounded wait is followed by a vote of the group (reducing barrier), so
 // that a timeout makes the whole group leave its loop together.
-constexpr int kChThreads = 384;
-constexpr int kChState = 256;  // state group: warps 0-7; epilogue group: warps 8-11
+constexpr int kChThreads = 512;
+constexpr int kChState = 256;  // state group: warps 0-7; epilogue group: warps 8-15
+constexpr int kChEpi = kChThreads - kChState;
 constexpr uint32_t kChBuf0 = 0;
 constexpr uint32_t kChBuf1 = kWsStride;
-constexpr uint32_t kChId = 2 * kWsStride;            // [I; 0] B operand [128 x 64] fp16
-constexpr uint32_t kChE = kChId + 16384;             // fp32 [64][kEStride] epilogue
+constexpr uint32_t kChE = 2 * kWsStride;             // fp32 [64][kEStride] epilogue
 constexpr int kEStride = kD + 4;
-constexpr uint32_t kChSmem = kChE + kC * kEStride * 4 + 1024;
+constexpr uint32_t kChG = kChE + kC * kEStride * 4;  // gate rows, bf16 [2][64][128]
+constexpr uint32_t kChSmem = kChG + 2 * kC * kD * 2 + 1024;
+static_assert(kChSmem <= 227 * 1024, "chain kernel shared memory");
 
 // TMEM columns: S^T fp32; [U^T | O^T] fp32 in two buffers; -S^T fp16 operand;
 // U^T fp16 operand in two buffers
 constexpr uint32_t kTS = 0, kTUO0 = 128, kTAS = 384, kTAU0 = 448;
 constexpr uint32_t kBarState = 1, kBarEpi = 2;  // named barriers of the two groups
-constexpr int kIssuer = kChState;  // epilogue thread that issues the loads and init MMAs
+constexpr int kLoader = kChState;  // epilogue thread that issues the bulk loads
 
 // Hardware tanh (tanh.approx.f32, maximum relative error about 2^-11); the
 // gate uses sigmoid(x) = (1 + tanh(x / 2)) / 2, one MUFU operation per value.
@@ -740,7 +740,7 @@ __device__ __forceinline__ float tanh_approx(float x) {
 
 __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_full[2], bar_init[2], bar_u, bar_s, bar_o[2], bar_dbg, bar_drain;
+  __shared__ uint64_t bar_full[2], bar_u, bar_s, bar_o[2], bar_oe[2], bar_dbg;
   __shared__ uint32_t tmem_base;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -764,10 +764,9 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     mbar_init(&bar_s, 1);
     mbar_init(&bar_o[0], 1);
     mbar_init(&bar_o[1], 1);
-    mbar_init(&bar_init[0], 1);
-    mbar_init(&bar_init[1], 1);
+    mbar_init(&bar_oe[0], 1);  // O^T of the buffer copied out by the epilogue
+    mbar_init(&bar_oe[1], 1);
     mbar_init(&bar_dbg, 1);
-    mbar_init(&bar_drain, 1);
     mbar_fence_init();
   }
   __syncthreads();
@@ -780,17 +779,6 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
   }
-  // [I; 0]: rows 0..63 the identity, rows 64..127 zero
-  for (int e = tid; e < 128 * 8; e += kChThreads) {
-    const int r = e >> 3, c8 = e & 7;
-    uint32_t w[4] = {0, 0, 0, 0};
-    if (r < 64 && (r >> 3) == c8) w[(r & 7) >> 1] = (r & 1) ? 0x3C000000u : 0x00003C00u;
-    *reinterpret_cast<uint4*>(sm + kChId + sw128_chunk(r, c8, 128)) =
-        make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  fence_proxy_async();  // the MMAs read the [I; 0] tile
-  // The bulk loads of the chunk blocks and the [U^T | O^T] = U~^T [I | 0] MMAs
-  // are issued by one epilogue thread (kIssuer), off the state chain.
   auto issue_load = [&](int i) {
     uint8_t* dst = sm + ((i & 1) ? kChBuf1 : kChBuf0);
     const uint8_t* src = ws_block(t, cbase + i, h);
@@ -798,8 +786,8 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     for (int p = 0; p < kWsParts; ++p)
       bulk_g2s(dst + kWsPartOff[p], src + kWsPartOff[p], kWsPartLen[p], &bar_full[i & 1]);
   };
-  int issued = 0, landed = 0;  // kIssuer: loads issued / loads seen complete
-  if (tid == kIssuer) {
+  int issued = 0;  // loads issued (kLoader)
+  if (tid == kLoader) {
     for (int i = 0; i < 2 && i < nchunks; ++i) issue_load(i);
     issued = min(2, nchunks);
   }
@@ -830,63 +818,76 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       ok = named_sync_and(kBarState, kChState, w);
       if (!ok) break;
       fence_after_sync();
-      // -S^T (fp16) into the A operand, S^T Diag(G_C) back into the accumulator
+      // -S^T (fp16) into the A operand of the product below
+      const float4* gam4 = reinterpret_cast<const float4*>(buf + kWsGam) + 16 * chalf;
+      uint32_t x0[32], x1[32];
+      tmem_ld32(lane_base + kTS + 64 * chalf, x0);
+      tmem_ld32(lane_base + kTS + 64 * chalf + 32, x1);
+      tmem_wait_ld();
       {
-        const float4* gam4 = reinterpret_cast<const float4*>(buf + kWsGam) + 16 * chalf;
-        uint32_t x0[32], x1[32], pk[32];
-        tmem_ld32(lane_base + kTS + 64 * chalf, x0);
-        tmem_ld32(lane_base + kTS + 64 * chalf + 32, x1);
-        tmem_wait_ld();
+        uint32_t pk[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 16; ++j)
           pk[j] = pack_half2(-__uint_as_float(x0[2 * j]), -__uint_as_float(x0[2 * j + 1]));
-          pk[16 + j] = pack_half2(-__uint_as_float(x1[2 * j]), -__uint_as_float(x1[2 * j + 1]));
-        }
-        tmem_st32(lane_base + kTAS + 32 * chalf, pk);
+        tmem_st16(lane_base + kTAS + 32 * chalf, pk);
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 g0 = gam4[j4], g1 = gam4[8 + j4];
-          x0[4 * j4 + 0] = __float_as_uint(__uint_as_float(x0[4 * j4 + 0]) * g0.x);
-          x0[4 * j4 + 1] = __float_as_uint(__uint_as_float(x0[4 * j4 + 1]) * g0.y);
-          x0[4 * j4 + 2] = __float_as_uint(__uint_as_float(x0[4 * j4 + 2]) * g0.z);
-          x0[4 * j4 + 3] = __float_as_uint(__uint_as_float(x0[4 * j4 + 3]) * g0.w);
-          x1[4 * j4 + 0] = __float_as_uint(__uint_as_float(x1[4 * j4 + 0]) * g1.x);
-          x1[4 * j4 + 1] = __float_as_uint(__uint_as_float(x1[4 * j4 + 1]) * g1.y);
-          x1[4 * j4 + 2] = __float_as_uint(__uint_as_float(x1[4 * j4 + 2]) * g1.z);
-          x1[4 * j4 + 3] = __float_as_uint(__uint_as_float(x1[4 * j4 + 3]) * g1.w);
-        }
-        tmem_st32(lane_base + kTS + 64 * chalf, x0);
-        tmem_st32(lane_base + kTS + 64 * chalf + 32, x1);
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_half2(-__uint_as_float(x1[2 * j]), -__uint_as_float(x1[2 * j + 1]));
+        tmem_st16(lane_base + kTAS + 32 * chalf + 16, pk);
         tmem_wait_st();
       }
       fence_before_sync();
       named_sync(kBarState, kChState);
-      bool winit = true;
+      bool woe = true;
       if (tid == 0) {
         fence_after_sync();
-        // [U^T | O^T] = U~^T [I | 0] must be in place (issued by kIssuer)
-        winit = mbar_wait(&bar_init[i & 1], (i >> 1) & 1, t.spins);
-        fence_after_sync();
+        // the product overwrites [U | O] buffer i & 1: O^T(i - 2) must be copied out
+        if (i >= 2) woe = mbar_wait(&bar_oe[i & 1], ((i - 2) >> 1) & 1, t.spins);
         const uint64_t dWQ = desc_k_sw128(smem_u32(buf) + kWsWQ, 0);
-        // [U^T | O^T] += (-S^T) [W ; -Q~]^T.  K-step: +2 in the descriptor's
+        // [U^T - U~^T | O^T] = (-S^T) [W ; -Q~]^T.  K-step: +2 in the descriptor's
         // address field (32 bytes); K-block of 64: +1024 (16 KB)
-        if (winit) {
+        if (woe) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N128, 1);
+            mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N128,
+                   ks > 0);
         }
         mma_commit(&bar_u);
       }
-      ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_u, i & 1, t.spins) && winit);
+      // S^T <- S^T Diag(G_C) while the product runs (only S^T += U^T K^ below
+      // reads it; the wait before that barrier covers these stores)
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 g0 = gam4[j4], g1 = gam4[8 + j4];
+        x0[4 * j4 + 0] = __float_as_uint(__uint_as_float(x0[4 * j4 + 0]) * g0.x);
+        x0[4 * j4 + 1] = __float_as_uint(__uint_as_float(x0[4 * j4 + 1]) * g0.y);
+        x0[4 * j4 + 2] = __float_as_uint(__uint_as_float(x0[4 * j4 + 2]) * g0.z);
+        x0[4 * j4 + 3] = __float_as_uint(__uint_as_float(x0[4 * j4 + 3]) * g0.w);
+        x1[4 * j4 + 0] = __float_as_uint(__uint_as_float(x1[4 * j4 + 0]) * g1.x);
+        x1[4 * j4 + 1] = __float_as_uint(__uint_as_float(x1[4 * j4 + 1]) * g1.y);
+        x1[4 * j4 + 2] = __float_as_uint(__uint_as_float(x1[4 * j4 + 2]) * g1.z);
+        x1[4 * j4 + 3] = __float_as_uint(__uint_as_float(x1[4 * j4 + 3]) * g1.w);
+      }
+      tmem_st32(lane_base + kTS + 64 * chalf, x0);
+      tmem_st32(lane_base + kTS + 64 * chalf + 32, x1);
+      // U~^T (this thread's row, its 32 columns) from the chunk block meanwhile
+      uint4 ut[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ut[c] = *reinterpret_cast<const uint4*>(buf + kWsUt + sw128_chunk(row, 4 * chalf + c, 128));
+      ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_u, i & 1, t.spins) && woe);
       if (!ok) break;
       fence_after_sync();
-      {  // U^T -> fp16 A operand (column half per warp)
+      {  // U^T = U~^T + the product -> fp16 A operand (column half per warp)
         uint32_t x0[32], pk[16];
         tmem_ld32(lane_base + (tUO - tmem) + 32 * chalf, x0);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[j] = pack_half2(__uint_as_float(x0[2 * j]), __uint_as_float(x0[2 * j + 1]));
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t hw = (&ut[j >> 2].x)[j & 3];
+          const float2 u2 = __half22float2(*reinterpret_cast<const __half2*>(&hw));
+          pk[j] = pack_half2(__uint_as_float(x0[2 * j]) + u2.x, __uint_as_float(x0[2 * j + 1]) + u2.y);
+        }
         tmem_st16(lane_base + tAU + 16 * chalf, pk);
         tmem_wait_st();
       }
@@ -929,86 +930,87 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     }
   } else {
     // ---------------- epilogue warps: O^T (lane = d_v) -> E[t][d_v] -> rows of y.
-    // Two threads own one token row (64 channels each).
-    const int et = tid - kChState;            // 0..127
-    const int er = et >> 1, eh = et & 1;      // token row, half of the channels
+    // Warp 8 + 4 ehalf + quarter copies columns t = 32 ehalf .. +31 of its lane
+    // quarter.  Four threads own one token row: thread (er, eq) takes the
+    // 8-channel groups q = eq + 4c, c = 0..3.
+    const int et = tid - kChState;            // 0..255
+    const int er = et >> 2, eq = et & 3;      // token row, channel-group phase
+    const int ehalf = (warp - 8) >> 2;
     const __nv_bfloat16* gate = static_cast<const __nv_bfloat16*>(a.gate);
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.o);
     float* E = reinterpret_cast<float*>(sm + kChE);
-    // kIssuer: [U^T | O^T](i) = U~^T [I | 0] once chunk i's block has landed
-    auto issue_init = [&](int i) {
-      const uint8_t* buf = sm + ((i & 1) ? kChBuf1 : kChBuf0);
-      const uint32_t tUO = tmem + kTUO0 + 128 * (i & 1);
-      const uint64_t dUt = desc_k_sw128(smem_u32(buf) + kWsUt, 0);
-      const uint64_t dId = desc_k_sw128(smem_u32(sm + kChId), 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) mma_ss(tUO, dUt + 2 * ks, dId + 2 * ks, kIdF16N128, ks > 0);
-      mma_commit(&bar_init[i & 1]);
+    // The gate rows stream into a two-slot ring by 16-byte asynchronous copies,
+    // two chunks ahead; each thread copies exactly the 64 bytes it reads later
+    // (16-byte group q of row er sits at position (q + 4 (er & 1)) mod 16, so
+    // the reads of a warp fall in distinct banks).
+    auto gate_slot = [&](int i, int c) -> uint32_t {
+      const int q = eq + 4 * c;
+      return kChG + (i & 1) * (kC * kD * 2) + er * (kD * 2) + (((q + 4 * (er & 1)) & 15) << 4);
     };
-    bool iss_ok = true;
-    if (tid == kIssuer) {
-      for (int i = 0; i < 2 && i < nchunks && iss_ok; ++i) {
-        iss_ok = mbar_wait(&bar_full[i & 1], (i >> 1) & 1, t.spins);
-        if (iss_ok) {
-          landed = i + 1;
-          issue_init(i);
-        }
+    auto fetch_gate = [&](int i) {
+      if (gate && i < nchunks) {
+        const int tok0 = s0 + i * kC;
+        const bool live = er < min(kC, s1 - tok0);
+        const __nv_bfloat16* src = gate + ((size_t)(tok0 + (live ? er : 0)) * H + h) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          cp_async16(smem_u32(sm + gate_slot(i, c)), src + 8 * (eq + 4 * c), live ? 16u : 0u);
       }
-    }
+      cp_async_commit();  // one group per chunk, empty or not
+    };
+    fetch_gate(0);
+    fetch_gate(1);
     for (int i = 0; i < nchunks; ++i) {
       const int tok0 = s0 + i * kC;
       const int len = min(kC, s1 - tok0);
       const bool live = er < len;
-      const size_t gofs = ((size_t)(tok0 + er) * H + h) * kD + 64 * eh;
-      uint4 graw[8];
-      if (gate && live) {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) graw[c] = *reinterpret_cast<const uint4*>(gate + gofs + 8 * c);
-      }
-      ok = named_sync_and(kBarEpi, 128,
-                          mbar_wait(&bar_o[i & 1], (i >> 1) & 1, t.spins) && iss_ok);
+      const size_t rofs = ((size_t)(tok0 + er) * H + h) * kD;
+      ok = named_sync_and(kBarEpi, kChEpi, mbar_wait(&bar_o[i & 1], (i >> 1) & 1, t.spins));
       if (!ok) {
         if (et == 0) report(a.status, KDA_ERR_TIMEOUT);
         break;
       }
       fence_after_sync();
-      if (tid == kIssuer && i + 2 < nchunks) {  // every MMA of chunk i is done: its
+      if (tid == kLoader && i + 2 < nchunks) {  // every MMA of chunk i is done: its
         fence_proxy_async();                    // buffer takes chunk i + 2
         issue_load(i + 2);
         issued = i + 3;
       }
       {
-        uint32_t x0[32], x1[32];
-        const uint32_t tO = lane_base + kTUO0 + 128 * (i & 1) + 64;
-        tmem_ld32(tO, x0);
-        tmem_ld32(tO + 32, x1);
+        uint32_t x0[32];
+        tmem_ld32(lane_base + kTUO0 + 128 * (i & 1) + 64 + 32 * ehalf, x0);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          E[j * kEStride + row] = __uint_as_float(x0[j]);
-          E[(32 + j) * kEStride + row] = __uint_as_float(x1[j]);
-        }
+        for (int j = 0; j < 32; ++j) E[(32 * ehalf + j) * kEStride + row] = __uint_as_float(x0[j]);
       }
       fence_before_sync();
-      named_sync(kBarEpi, 128);  // O^T(i) is out of TMEM: the [U|O] buffer may be reused
+      named_sync(kBarEpi, kChEpi);
+      if (et == 0) mbar_arrive(&bar_oe[i & 1]);  // O^T(i) is out of TMEM: the buffer is free
       // pass 1: sum of squares of the row; pass 2: outputs, 8 channels at a time
-      const float4* er4 = reinterpret_cast<const float4*>(&E[er * kEStride + 64 * eh]);
+      const float* erow = E + er * kEStride;
       float ss = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v4 = er4[c];
-        ss += v4.x * v4.x + v4.y * v4.y + v4.z * v4.z + v4.w * v4.w;
+      for (int c = 0; c < 4; ++c) {
+        const float4 v0 = *reinterpret_cast<const float4*>(erow + 8 * (eq + 4 * c));
+        const float4 v1 = *reinterpret_cast<const float4*>(erow + 8 * (eq + 4 * c) + 4);
+        ss += v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w;
+        ss += v1.x * v1.x + v1.y * v1.y + v1.z * v1.z + v1.w * v1.w;
       }
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       const float inv = gate ? rsqrtf(ss * (1.0f / kD) + a.eps_norm) : 1.f;
       const float hinv = 0.5f * inv;  // inv * sigmoid(g) = hinv * tanh(g / 2) + hinv
+      cp_async_wait_group<1>();       // this thread's gate copies of chunk i have landed
       if (live) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 v0 = er4[2 * c], v1 = er4[2 * c + 1];
+        for (int c = 0; c < 4; ++c) {
+          const int q = eq + 4 * c;
+          const float4 v0 = *reinterpret_cast<const float4*>(erow + 8 * q);
+          const float4 v1 = *reinterpret_cast<const float4*>(erow + 8 * q + 4);
           float y[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           if (gate) {
-            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw[c]);
+            const uint4 graw = *reinterpret_cast<const uint4*>(sm + gate_slot(i, c));
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const float2 gf = __bfloat1622float2(g2[u]);
@@ -1016,7 +1018,7 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
               y[2 * u + 1] *= fmaf(tanh_approx(0.5f * gf.y), hinv, hinv);
             }
             if (a.norm_weight) {
-              const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 64 * eh + 8 * c);
+              const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 8 * q);
               const float4 w0 = w4[0], w1 = w4[1];
               y[0] *= w0.x; y[1] *= w0.y; y[2] *= w0.z; y[3] *= w0.w;
               y[4] *= w1.x; y[5] *= w1.y; y[6] *= w1.z; y[7] *= w1.w;
@@ -1027,26 +1029,18 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
           out.y = pack_bf162(y[2], y[3]);
           out.z = pack_bf162(y[4], y[5]);
           out.w = pack_bf162(y[6], y[7]);
-          *reinterpret_cast<uint4*>(o + gofs + 8 * c) = out;
+          *reinterpret_cast<uint4*>(o + rofs + 8 * q) = out;
         }
       }
-      if (tid == kIssuer && i + 2 < nchunks) {
-        fence_after_sync();
-        iss_ok = mbar_wait(&bar_full[i & 1], ((i + 2) >> 1) & 1, t.spins);
-        if (iss_ok) {
-          landed = i + 3;
-          issue_init(i + 2);
-        }
-      }
-      named_sync(kBarEpi, 128);  // E is free again
+      fetch_gate(i + 2);  // slot i & 1 is read: it takes chunk i + 2
+      named_sync(kBarEpi, kChEpi);  // E is free again
     }
-    if (tid == kIssuer && (!ok || !iss_ok)) {
-      // a bounded wait gave up: wait (bounded) for this thread's own MMAs and
-      // bulk copies before TMEM and shared memory are released
-      report(a.status, KDA_ERR_TIMEOUT);
-      mma_commit(&bar_drain);
-      mbar_wait(&bar_drain, 0, t.spins);
-      for (int j = landed; j < issued; ++j) mbar_wait(&bar_full[j & 1], (j >> 1) & 1, t.spins);
+    cp_async_wait_all();  // no copy into shared memory outlives the loop
+    if (tid == kLoader && !ok) {
+      // a bounded wait gave up: the last two loads may still be in flight; wait
+      // (bounded) for them before shared memory is released
+      for (int j = max(0, issued - 2); j < issued; ++j)
+        mbar_wait(&bar_full[j & 1], (j >> 1) & 1, t.spins);
     }
   }
   fence_before_sync();

@@ -262,6 +262,11 @@ __device__ __forceinline__ void cp_async_commit() {
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
+// Wait until at most N of this thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------ packing
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
