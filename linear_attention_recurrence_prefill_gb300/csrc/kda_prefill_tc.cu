@@ -164,20 +164,22 @@ constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
 constexpr uint32_t kPrepAhi = kPrepX, kPrepAlo = kPrepX + 16384;
 constexpr uint32_t kPrepBhi = kPrepX + 32768, kPrepBlo = kPrepX + 34816;
 //   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64] with padded row
-//   strides (no bank conflicts between the rows a warp touches), 3 KB scratch
+//   strides (no bank conflicts between the rows a warp touches), 4 KB scratch
 constexpr int kAs = 66, kXs = 68;  // row strides (floats) of A and of the inverse
 constexpr uint32_t kPrepAmat = kPrepX, kPrepInv = kPrepX + kC * kAs * 4;
 constexpr uint32_t kPrepY = kPrepInv + kC * kXs * 4;
-//   W / U~ MMAs: [T; T] [128 (t) x 64 (j)] fp16 K-major over A; V and K~ [64 (j) rows
-//   of 128 channels] fp16 MN-major over the q and k rows
+//   W / U~ MMAs: [T; T] [128 (t) x 64 (j)] fp16 K-major over A; V (bf16) and K~
+//   (fp16) [64 (j) rows of 128 channels] MN-major over the q and k rows
 constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
+//   T as bf16 hi/lo K-major [64 (t)][64 (j)] tiles over the decay rows
+constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
 // TMEM: Gram D in columns 0..63, then U~^T (64 columns) and W (128 columns)
 constexpr uint32_t kPrepTmemCols = 256, kTdU = 0, kTdW = 64;
-constexpr uint32_t kIdUt = idesc_f16(128, 64, false, true, false);  // A MN-major, N = 64
+constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
-static_assert(kPrepY + 3 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
+static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
 static_assert(kPrepBlo + 2048 <= kPrepSmall, "Gram operands inside the reused region");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
 static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
@@ -199,9 +201,16 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
   }
 }
 
-__device__ __forceinline__ void ld8f(const float* p, float (&f)[8]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0];
-  const float4 b = reinterpret_cast<const float4*>(p)[1];
+// Decay rows in shared memory keep the two halves of each 8-channel group c in
+// separate 256-byte halves of the 512-byte row (channels 8c .. 8c+3 at float
+// 4c, channels 8c+4 .. 8c+7 at float 64 + 4c), so that threads reading
+// consecutive groups touch consecutive 16-byte words.
+__host__ __device__ constexpr int gpos(int ch) { return ((ch >> 2) & 1) * 64 + (ch >> 3) * 4 + (ch & 3); }
+
+// 8-channel group c of a decay row
+__device__ __forceinline__ void ld8g(const float* row, int c, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(row + 4 * c);
+  const float4 b = *reinterpret_cast<const float4*>(row + 64 + 4 * c);
   f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
@@ -295,7 +304,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       const int w2 = e - 2048;
       r = w2 >> 5;
       col16 = w2 & 31;
-      dst = smem_u32(sm + kPrepG + r * 512 + col16 * 16);
+      // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
+      dst = smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + (col16 >> 1) * 16);
       src = reinterpret_cast<const char*>(a.log_alpha);
     }
     const int rr = r < len ? r : 0;
@@ -319,7 +329,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 
   // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
   //      registers); L2 norms of the q, k rows (warps 4-7, four rows at a time) ----
-  if (tid < kD) {
+  if (tid < kD) {  // thread tid scans word tid of the rows (whichever channel it holds)
     float x[kC];
 #pragma unroll
     for (int r = 0; r < kC; ++r) x[r] = G[r * kD + tid];
@@ -370,7 +380,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   for (int round = 0; round < 8; ++round) {
     const int b = round >> 1, kh = round & 1;
     const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group), then 128 B items
-    const float* gend = G + (16 * b + 15) * kD + 64 * kh;
+    // the decay at the end of tile b, for this thread's channel group (every
+    // item of this thread has the same group, 8 kh + tid % 8)
+    float ge[8];
+    ld8g(G + (16 * b + 15) * kD, 8 * kh + (tid & 7), ge);
     uint4 iv0[3], iv1[3], iv2[3], iv3[3];
     uint32_t io0[3], io1[3];
     int kind[3];  // 0: none, 1: A item, 2: B item
@@ -381,9 +394,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       if (kind[s] == 1) {
         const int r = 16 * b + (it >> 3), c8 = it & 7;
         const int ch = 64 * kh + 8 * c8;
-        float g8[8], ge[8], kf[8], qf[8];
-        ld8f(G + r * kD + ch, g8);
-        ld8f(gend + 8 * c8, ge);
+        float g8[8], kf[8], qf[8];
+        ld8g(G + r * kD, 8 * kh + c8, g8);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
         const float ik = s_invk[r], iq = s_invq[r];
@@ -406,9 +418,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       } else if (kind[s] == 2) {
         const int e = it - nA, jj = e >> 3, c8 = e & 7;
         const int j = 16 * b + jj, ch = 64 * kh + 8 * c8;
-        float g8[8], ge[8], kf[8];
-        ld8f(G + j * kD + ch, g8);
-        ld8f(gend + 8 * c8, ge);
+        float g8[8], kf[8];
+        ld8g(G + j * kD, 8 * kh + c8, g8);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + ch * 2), kf);
         const float ik = s_invk[j];
         const float2 ik2 = make_float2(ik, ik);
@@ -505,84 +516,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     fence_before_sync();
     __syncthreads();
 
-    // v rows for the V operand of step 7, fetched now so that the loads overlap
-    // the solve: item (token j, 8-channel group c16) = tid + 256 m
-    uint4 vreg[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int e = tid + kPrepThreads * m, j = e >> 4, c16 = e & 15;
-      vreg[m] = make_uint4(0u, 0u, 0u, 0u);
-      if (j < len)
-        vreg[m] = __ldg(reinterpret_cast<const uint4*>(v + ((size_t)(tok0 + j) * H + h) * kD) + c16);
-    }
-
-    // ---- 5. X = (I + A)^-1 by 16 x 16 blocks ----
-    float* X = reinterpret_cast<float*>(sm + kPrepInv);
-    float* Y = reinterpret_cast<float*>(sm + kPrepY);
-    for (int e = tid; e < kC * kXs; e += kPrepThreads) X[e] = 0.f;
-    __syncthreads();
-    if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc)
-      const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < r; ++m) acc -= Amat[(o + r) * kAs + o + m] * x[m];
-        x[r] = acc;
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
-    }
-    __syncthreads();
-    // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj;
-    // each thread computes 4 adjacent columns of one row (float4 loads of X, Y)
-    for (int dd = 1; dd < 4; ++dd) {
-      const int nblk = 4 - dd;
-      for (int e = tid; e < nblk * 64; e += kPrepThreads) {
-        const int bj = e >> 6, bi = bj + dd, r = (e >> 2) & 15, c4 = (e & 3) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* arow = Amat + (16 * bi + r) * kAs;
-        for (int m = 16 * bj; m < 16 * bi; ++m) {
-          const float am = arow[m];
-          const float4 x4 = *reinterpret_cast<const float4*>(X + m * kXs + 16 * bj + c4);
-          acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
-        }
-        *reinterpret_cast<float4*>(Y + (bj << 8) + r * 16 + c4) = acc;
-      }
-      __syncthreads();
-      for (int e = tid; e < nblk * 64; e += kPrepThreads) {
-        const int bj = e >> 6, bi = bj + dd, r = (e >> 2) & 15, c4 = (e & 3) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float xm = xrow[m];
-          const float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
-          acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
-        }
-        *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-      }
-      __syncthreads();
-    }
-
-    // ---- 6. [T; T] tile (K-major [t][j] fp16, rows 64..127 repeat rows 0..63) over
-    //      A; row pass: K~ and V held for step 7, -Q~ rows, K^ rows and G_C straight
-    //      to the workspace.  Row item (row r, 8-channel group c16) = tid + 256 m ----
-    for (int e = tid; e < kC * 8; e += kPrepThreads) {
-      const int tr = e >> 3, c8 = e & 7;
-      uint32_t w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j0 = 8 * c8 + 2 * u;
-        const float2 x2 = *reinterpret_cast<const float2*>(X + tr * kXs + j0);
-        w[u] = pack_half2(x2.x * s_beta[j0], x2.y * s_beta[j0 + 1]);
-      }
-      const uint4 wt = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(tr, c8, 128)) = wt;
-      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(kC + tr, c8, 128)) = wt;
-    }
+    // ---- 5. row pass: -Q~ rows, K^ rows and G_C straight to the workspace, K~
+    //      (fp16) into the MN-major operand over the k rows; then the v rows, by
+    //      16-byte asynchronous copies (bf16, landing during the solve), into the
+    //      MN-major operand over the q rows.  Row item (row r, 8-channel group
+    //      c16) = tid + 256 m ----
     uint4 ktl[4];
     {
       const float* Gl = G + (kC - 1) * kD;
@@ -590,8 +528,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       for (int m = 0; m < 4; ++m) {
         const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
         float g8[8], gl8[8], kf[8], qf[8];
-        ld8f(G + r * kD + ch, g8);
-        ld8f(Gl + ch, gl8);
+        ld8g(G + r * kD, c16, g8);
+        ld8g(Gl, c16, gl8);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
         unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
         const float ik = s_invk[r], iq = -s_invq[r];
@@ -616,38 +554,132 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
             make_uint4(wh[0], wh[1], wh[2], wh[3]);
       }
-      if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(Gl[tid]);
+      if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(Gl[gpos(tid)]);
     }
     __syncthreads();  // every read of the q and k rows is done: their space takes K~ and V
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15;
       *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = ktl[m];
-      const uint32_t* vb = reinterpret_cast<const uint32_t*>(&vreg[m]);
-      uint32_t wv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        wv[u] = pack_half2(__uint_as_float(vb[u] << 16), __uint_as_float(vb[u] & 0xFFFF0000u));
-      *reinterpret_cast<uint4*>(sm + kPrepV + sw128_chunk(r, c16, kC)) =
-          make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      const int rr = r < len ? r : 0;
+      cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
+                 v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
     }
+    cp_async_commit();
+
+    // ---- 6. X = (I + A)^-1 by 16 x 16 blocks ----
+    float* X = reinterpret_cast<float*>(sm + kPrepInv);
+    float* Y = reinterpret_cast<float*>(sm + kPrepY);
+    if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
+      const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update rows
+      float x[16];                                          // below: a 15-FMA chain)
+#pragma unroll
+      for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m) {
+#pragma unroll
+        for (int r = m + 1; r < 16; ++r) x[r] -= Amat[(o + r) * kAs + o + m] * x[m];
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
+    } else {  // the blocks above the diagonal are zero
+      for (int e = tid - 64; e < 6 * 256; e += kPrepThreads - 64) {
+        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
+      }
+    }
+    __syncthreads();
+    // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj.
+    // The sum is split by 16-token tile p of m: one unrolled 16-term product per
+    // thread (4 adjacent columns of one row, float4 loads), partial sums in Y.
+#pragma unroll
+    for (int dd = 1; dd < 4; ++dd) {
+      const int nblk = 4 - dd;
+      if (tid < nblk * dd * 64) {
+        const int p = tid / (nblk * 64), rem = tid - p * (nblk * 64);
+        const int bj = rem >> 6, bi = bj + dd, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
+        const int m0 = 16 * (bj + p);
+        const float* arow = Amat + (16 * bi + r) * kAs + m0;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int mm = 0; mm < 16; ++mm) {
+          const float am = arow[mm];
+          const float4 x4 = *reinterpret_cast<const float4*>(X + (m0 + mm) * kXs + 16 * bj + c4);
+          acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+        }
+        *reinterpret_cast<float4*>(Y + ((p * nblk + bj) << 8) + r * 16 + c4) = acc;
+      }
+      __syncthreads();
+      if (tid < nblk * 64) {
+        const int bj = tid >> 6, bi = bj + dd, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const float xm = xrow[m];
+          float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
+#pragma unroll
+          for (int pp = 1; pp < dd; ++pp) {
+            const float4 z4 =
+                *reinterpret_cast<const float4*>(Y + ((pp * nblk + bj) << 8) + m * 16 + c4);
+            y4.x += z4.x; y4.y += z4.y; y4.z += z4.z; y4.w += z4.w;
+          }
+          acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
+        }
+        *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+      }
+      __syncthreads();
+    }
+
+    // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
+    //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
+    //      decay rows for the U~ product (V stays exact in bf16) ----
+    for (int e = tid; e < kC * 8; e += kPrepThreads) {
+      const int tr = e >> 3, c8 = e & 7;
+      uint32_t w[4], th[4], tl[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j0 = 8 * c8 + 2 * u;
+        const float2 x2 = *reinterpret_cast<const float2*>(X + tr * kXs + j0);
+        const float2 t2 = make_float2(x2.x * s_beta[j0], x2.y * s_beta[j0 + 1]);
+        w[u] = pack_half2(t2.x, t2.y);
+        split2v(t2, th[u], tl[u]);
+      }
+      const uint4 wt = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(tr, c8, 128)) = wt;
+      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(kC + tr, c8, 128)) = wt;
+      *reinterpret_cast<uint4*>(sm + kPrepThi + sw128_chunk(tr, c8, kC)) =
+          make_uint4(th[0], th[1], th[2], th[3]);
+      *reinterpret_cast<uint4*>(sm + kPrepTlo + sw128_chunk(tr, c8, kC)) =
+          make_uint4(tl[0], tl[1], tl[2], tl[3]);
+    }
+    cp_async_wait_all();  // this thread's v rows have landed
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
 
-    // ---- 7. U~^T = V^T T^T (A = V MN-major, B = T) and W = [T; T] K~ (B = K~
-    //      MN-major) on the tensor cores, then both straight to the workspace ----
+    // ---- 8. U~^T = V^T (T_hi + T_lo)^T (A = V MN-major bf16) and W = [T; T] K~
+    //      (B = K~ MN-major fp16) on the tensor cores, then both straight to the
+    //      workspace ----
     if (tid == 0) {
       fence_after_sync();
       const uint32_t sT = smem_u32(sm + kPrepTT), sV = smem_u32(sm + kPrepV);
       const uint32_t sKt = smem_u32(sm + kPrepKt);
+      const uint32_t sTh = smem_u32(sm + kPrepThi), sTl = smem_u32(sm + kPrepTlo);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sT, 32 * ks),
+        mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTh, 32 * ks),
                kIdUt, ks > 0);
         mma_ss(tmem + kTdW, desc_k_sw128(sT, 32 * ks), desc_mn_sw128(sKt, ks, kC * 128),
                kIdW, ks > 0);
       }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTl, 32 * ks),
+               kIdUt, 1u);
       mma_commit(&bar_mma);
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
