@@ -76,11 +76,12 @@ def kernel_plan(path: str, chunk: int):
         prep_b = (3 * 2 * D + 4 * D + 2) * T * H + ws
         # chain: reads the blocks and the gate, writes y, reads S0 and writes S_T
         chain_b = ws + 2 * 2 * D * T * H + 2 * STATE_BYTES * H
-        # tensor-core flops issued per (chunk, head): Gram 3 x 4 x (128x16x128),
-        # W and U~ 2 x (128x64x64); chain 7 products of 128 x (64|128) x (64|128)
-        prep_f = (3 * 4 * 2 * 128 * 16 * 128 + 2 * 2 * 128 * 64 * 64) * chunks
-        chain_f = (2 * 128 * 64 * 64 + 2 * 2 * 128 * 64 * 128 + 2 * 128 * 64 * 64
-                   + 2 * 128 * 128 * 64) * chunks
+        # tensor-core flops issued per (chunk, head): Gram 3 x 4 x (128x16x128);
+        # U~ 2 x (128x64x64) (T as a bf16 hi/lo pair); W 128x128x64.  Chain:
+        # [D | O] 128x128x128, S += U K^ 128x128x64, O += U P^T 128x64x64
+        prep_f = (3 * 4 * 2 * 128 * 16 * 128 + 2 * 2 * 128 * 64 * 64
+                  + 2 * 128 * 128 * 64) * chunks
+        chain_f = (2 * 128 * 128 * 128 + 2 * 128 * 128 * 64 + 2 * 128 * 64 * 64) * chunks
         return [("chunk_base_kernel", "hbm", 4 * 2, 0.0),
                 ("prep_kernel", "hbm", prep_b, prep_f),
                 ("chain_kernel", "hbm", chain_b, chain_f)]
