@@ -66,6 +66,17 @@ enum {
   KDA_IMPL_TC = 2    /* tcgen05 tensor-core chunked path                    */
 };
 
+/* Decay modes.  KDA keeps one decay per key channel; Gated DeltaNet shrinks the
+ * whole state by one factor per head, and DeltaNet has no decay ("Kimi K3",
+ * section "Forgetting different features at different rates"; "Kimi K3's
+ * hybrid block, from first principles", section "From linear attention to the
+ * delta rule").  The recurrence is otherwise the same. */
+enum {
+  KDA_DECAY_CHANNEL = 0, /* log_alpha [..][H][d_k]: one decay per key channel   */
+  KDA_DECAY_HEAD = 1,    /* log_alpha [..][H]: one decay per token and head    */
+  KDA_DECAY_NONE = 2     /* alpha = 1; log_alpha is not read and may be NULL   */
+};
+
 /*
  * Options.  Always initialise with kda_options_init() and then override.
  */
@@ -90,6 +101,21 @@ typedef struct kda_options {
   void* const* phase_events; /* NULL, or (launches + 1) cudaEvent_t handles that
                             kda_prefill records on `stream` before each of its
                             kernels and after the last (per-kernel timing)      */
+  int decay_mode;        /* KDA_DECAY_*, default KDA_DECAY_CHANNEL.  With
+                            KDA_DECAY_HEAD, log_alpha needs only 4-byte
+                            alignment                                            */
+  int snapshot_every;    /* 0 (default): off.  Else a positive multiple of 64:
+                            kda_prefill also writes the state after every
+                            prefix of m * snapshot_every tokens of each
+                            sequence, for prefix caching ("What's new in Kimi
+                            K3", section "What it costs to serve": a KDA prefix
+                            can only be reused where its state was saved)     */
+  float* snapshots;      /* with snapshot_every: fp32
+                            [N][L / snapshot_every][H][d_k][d_v], L =
+                            max_seqlen (or T_total / N without cu_seqlens,
+                            T_total with them); slot m of sequence n holds
+                            the state after (m + 1) * snapshot_every of its
+                            tokens, slots past its length are not written   */
 } kda_options;
 
 /* Fill *opt with the defaults listed above. */
@@ -105,7 +131,8 @@ void kda_options_init(kda_options* opt);
  *
  *   q, k        [T_total][H][d_k]  dtype
  *   v           [T_total][H][d_v]  dtype
- *   log_alpha   [T_total][H][d_k]  fp32 (clamped to [g_min, 0] inside)
+ *   log_alpha   [T_total][H][d_k]  fp32 (clamped to [g_min, 0] inside);
+ *               [T_total][H] with KDA_DECAY_HEAD, unused with KDA_DECAY_NONE
  *   beta        [T_total][H]       dtype
  *   S0          [N][H][d_k][d_v]   fp32 initial states, NULL = zeros
  *   cu_seqlens  [N+1] int32 on the device, cu_seqlens[0] = 0,

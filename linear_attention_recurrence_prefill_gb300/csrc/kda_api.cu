@@ -35,6 +35,15 @@ bool beta_aligned(const void* p, int dtype) {
   return (reinterpret_cast<uintptr_t>(p) & (dtype == KDA_BF16 ? 1u : 3u)) == 0;
 }
 bool supported_d(int d) { return d == 32 || d == 64 || d == 128; }
+// log_alpha: required unless there is no decay; a per-head array is read one
+// element at a time
+bool log_alpha_ok(const float* la, int mode) {
+  return mode == KDA_DECAY_NONE || la != nullptr;
+}
+bool log_alpha_aligned(const float* la, int mode) {
+  if (!la || mode == KDA_DECAY_NONE) return true;
+  return mode == KDA_DECAY_HEAD ? (reinterpret_cast<uintptr_t>(la) & 3u) == 0 : aligned16(la);
+}
 
 const kda_options* opts_or_default(const kda_options* opt, kda_options* storage) {
   if (opt) return opt;
@@ -50,6 +59,7 @@ int check_common_opts(const kda_options* o) {
   if (!(o->g_min >= -5.0f && o->g_min <= 0.0f)) return KDA_ERR_ARG;
   if (!(o->eps_l2 >= 0.0f) || !(o->eps_norm >= 0.0f)) return KDA_ERR_ARG;
   if (o->q_scale != o->q_scale) return KDA_ERR_ARG;
+  if (o->decay_mode < KDA_DECAY_CHANNEL || o->decay_mode > KDA_DECAY_NONE) return KDA_ERR_ARG;
   if (o->gate && !aligned16(o->gate)) return KDA_ERR_ALIGN;
   if (o->norm_weight && !aligned16(o->norm_weight)) return KDA_ERR_ALIGN;
   return KDA_OK;
@@ -79,9 +89,10 @@ void kda_options_init(kda_options* opt) {
   opt->eps_l2 = 1e-6f;
   opt->eps_norm = 1e-6f;
   opt->impl = KDA_IMPL_AUTO;
+  opt->decay_mode = KDA_DECAY_CHANNEL;
 }
 
-int kda_abi_version(void) { return 1; }
+int kda_abi_version(void) { return 2; }
 
 const char* kda_status_string(int s) {
   switch (s) {
@@ -133,16 +144,18 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
   const kda_options* op = opts_or_default(opt, &def);
   if (N < 1 || H < 1 || T_total < 0) return KDA_ERR_SHAPE;
   // token arrays may be NULL only when there are no tokens
-  if (!S_T || (T_total > 0 && (!q || !k || !v || !log_alpha || !beta || !o)))
+  if (!S_T || (T_total > 0 && (!q || !k || !v || !log_alpha_ok(log_alpha, op->decay_mode) ||
+                               !beta || !o)))
     return KDA_ERR_ARG;
   if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
   if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
   if (!cu_seqlens && (T_total % N) != 0) return KDA_ERR_SHAPE;
   if (op->max_seqlen < 0 || op->max_seqlen > T_total) return KDA_ERR_SHAPE;
   if (op->chunk != 0 && op->chunk != 16 && op->chunk != 64) return KDA_ERR_ARG;
-  const void* ptrs[] = {q, k, v, log_alpha, o, S_T};
+  const void* ptrs[] = {q, k, v, o, S_T};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  if (!log_alpha_aligned(log_alpha, op->decay_mode)) return KDA_ERR_ALIGN;
   if (beta && !beta_aligned(beta, dtype)) return KDA_ERR_ALIGN;
   if ((S0 && !aligned16(S0)) || (cu_seqlens && !aligned16(cu_seqlens))) return KDA_ERR_ALIGN;
   int rc = check_common_opts(op);
@@ -150,6 +163,16 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
   // 64-bit extents: every index below 2^62
   const long long tok_elems = (long long)T_total * H * d_k;
   if (tok_elems < 0) return KDA_ERR_SHAPE;
+  // state snapshots every snapshot_every tokens (a multiple of the chunk)
+  int snap_slots = 0;
+  if (op->snapshot_every < 0 || (op->snapshot_every > 0 && op->snapshot_every % 64 != 0))
+    return KDA_ERR_ARG;
+  if (op->snapshot_every > 0) {
+    if (!op->snapshots) return KDA_ERR_ARG;
+    if (!aligned16(op->snapshots)) return KDA_ERR_ALIGN;
+    const int L = op->max_seqlen > 0 ? op->max_seqlen : (cu_seqlens ? T_total : T_total / N);
+    snap_slots = L / op->snapshot_every;
+  }
 
   const int path = prefill_path(op, d_k, dtype);
   if (path < 0) return KDA_ERR_UNSUPPORTED;
@@ -164,8 +187,12 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
   a.gate = op->gate; a.norm_weight = op->norm_weight; a.status = status;
   a.N = N; a.T_total = T_total; a.H = H; a.d = d_k;
   a.l2norm_qk = op->l2norm_qk; a.beta_is_logit = op->beta_is_logit;
+  a.decay_mode = op->decay_mode;
   a.g_min = op->g_min; a.q_scale = op->q_scale; a.eps_l2 = op->eps_l2;
   a.eps_norm = op->eps_norm;
+  a.snapshots = snap_slots > 0 ? op->snapshots : nullptr;
+  a.snapshot_every = op->snapshot_every;
+  a.snapshot_slots = snap_slots;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -188,13 +215,15 @@ int kda_decode_step(const void* q, const void* k, const void* v, const float* lo
                     int dtype, const kda_options* opt, kda_stream_t stream) {
   kda_options def;
   const kda_options* op = opts_or_default(opt, &def);
-  if (!q || !k || !v || !log_alpha || !beta || !S || !o) return KDA_ERR_ARG;
+  if (!q || !k || !v || !log_alpha_ok(log_alpha, op->decay_mode) || !beta || !S || !o)
+    return KDA_ERR_ARG;
   if (N < 1 || H < 1) return KDA_ERR_SHAPE;
   if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
   if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
-  const void* ptrs[] = {q, k, v, log_alpha, S, o};
+  const void* ptrs[] = {q, k, v, S, o};
   for (const void* p : ptrs)
     if (!aligned16(p)) return KDA_ERR_ALIGN;
+  if (!log_alpha_aligned(log_alpha, op->decay_mode)) return KDA_ERR_ALIGN;
   if (!beta_aligned(beta, dtype)) return KDA_ERR_ALIGN;
   int rc = check_common_opts(op);
   if (rc != KDA_OK) return rc;
@@ -205,6 +234,7 @@ int kda_decode_step(const void* q, const void* k, const void* v, const float* lo
   a.gate = op->gate; a.norm_weight = op->norm_weight;
   a.N = N; a.H = H; a.d = d_k;
   a.l2norm_qk = op->l2norm_qk; a.beta_is_logit = op->beta_is_logit;
+  a.decay_mode = op->decay_mode;
   a.g_min = op->g_min; a.q_scale = op->q_scale; a.eps_l2 = op->eps_l2;
   a.eps_norm = op->eps_norm;
   cudaError_t e = launch_decode(a, dtype, reinterpret_cast<cudaStream_t>(stream));

@@ -45,9 +45,19 @@ struct PrefillArgs {
   const float* norm_weight;
   int* status;
   int N, T_total, H, d;
-  int l2norm_qk, beta_is_logit;
+  int l2norm_qk, beta_is_logit, decay_mode;
   float g_min, q_scale, eps_l2, eps_norm;
+  float* snapshots;          // NULL: no state snapshots
+  int snapshot_every;        // tokens between snapshots (a multiple of 64)
+  int snapshot_slots;        // slots per sequence in `snapshots`
 };
+
+// Slot of the snapshot taken after `done` tokens of a sequence, or -1.
+__device__ __forceinline__ int snapshot_slot(const PrefillArgs& a, int done) {
+  if (!a.snapshots || done <= 0 || done % a.snapshot_every != 0) return -1;
+  const int m = done / a.snapshot_every - 1;
+  return m < a.snapshot_slots ? m : -1;
+}
 
 struct DecodeArgs {
   const void* q;
@@ -60,9 +70,18 @@ struct DecodeArgs {
   const void* gate;
   const float* norm_weight;
   int N, H, d;
-  int l2norm_qk, beta_is_logit;
+  int l2norm_qk, beta_is_logit, decay_mode;
   float g_min, q_scale, eps_l2, eps_norm;
 };
+
+// log alpha of token-head row `row` (token * H + head), key channel c, under
+// the decay mode (KDA_DECAY_*), before the floor.
+__device__ __forceinline__ float log_alpha_at(const float* la, int mode, size_t row, int d,
+                                              int c) {
+  if (mode == KDA_DECAY_CHANNEL) return la[row * d + c];
+  if (mode == KDA_DECAY_HEAD) return la[row];
+  return 0.f;
+}
 
 // Token range [t0, t1) of sequence n.
 __device__ __forceinline__ void seq_range(const int32_t* cu, int N, int T_total, int n,

@@ -49,7 +49,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
     sq[tid] = to_f32(q[base + tid]);
     sk[tid] = to_f32(k[base + tid]);
     sv[tid] = to_f32(v[base + tid]);
-    const float la = fminf(fmaxf(a.log_alpha[base + tid], a.g_min), 0.f);
+    const float la =
+        fminf(fmaxf(log_alpha_at(a.log_alpha, a.decay_mode, (size_t)unit, D, tid), a.g_min), 0.f);
     sa[tid] = expf(la);
   }
   __syncthreads();

@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillArgs a) {
         qv = to_f32(q[gi]);
         kv = to_f32(k[gi]);
         vv = to_f32(v[gi]);
-        la = fminf(fmaxf(a.log_alpha[gi], a.g_min), 0.f);
+        la = fminf(fmaxf(log_alpha_at(a.log_alpha, a.decay_mode, (size_t)tok * H + h, D, c),
+                         a.g_min), 0.f);
       }
       Qt[e] = qv;
       Kt[e] = kv;
@@ -296,6 +297,12 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillArgs a) {
       }
     }
     __syncthreads();
+    // state snapshot after a multiple of snapshot_every tokens
+    const int m = (c0 + kC <= t1) ? snapshot_slot(a, c0 + kC - t0) : -1;
+    if (m >= 0) {
+      float* dst = a.snapshots + (((size_t)n * a.snapshot_slots + m) * H + h) * (size_t)(D * D);
+      for (int e = tid; e < D * D; e += kThreads) dst[e] = S[e];
+    }
   }
 
   for (int e = tid; e < D * D; e += kThreads) a.S_T[sbase + e] = S[e];

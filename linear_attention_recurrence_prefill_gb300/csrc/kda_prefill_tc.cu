@@ -289,8 +289,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 
   // ---- 1. input rows by 16-byte asynchronous copies (all threads): q, k rows of
   //      256 B and log alpha rows of 512 B; rows past the sequence end are
-  //      zero-filled (an identity step) ----
-  for (int e = tid; e < kC * 64; e += kPrepThreads) {
+  //      zero-filled (an identity step).  With one decay per head (or none) the
+  //      decay rows are filled by broadcasting the row's value instead ----
+  const int n_copy = a.decay_mode == KDA_DECAY_CHANNEL ? kC * 64 : kC * 32;
+  for (int e = tid; e < n_copy; e += kPrepThreads) {
     const int reg = e >> 10, w = e & 1023;  // 0: q, 1: k, 2-3: log alpha
     int r, col16;
     uint32_t dst;
@@ -314,6 +316,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     cp_async16(dst, src, r < len ? 16u : 0u);
   }
   cp_async_commit();
+  if (a.decay_mode != KDA_DECAY_CHANNEL) {
+    for (int e = tid; e < kC * 32; e += kPrepThreads) {  // 16-byte words of the rows
+      const int r = e >> 5, w = e & 31;
+      const float g = (r < len && a.decay_mode == KDA_DECAY_HEAD)
+                          ? a.log_alpha[(size_t)(tok0 + r) * H + h] : 0.f;
+      *reinterpret_cast<float4*>(sm + kPrepG + r * 512 + w * 16) = make_float4(g, g, g, g);
+    }
+  }
   if (tid < kC) {
     float b = 0.f;
     if (tid < len) {
@@ -856,6 +866,18 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       tmem_ld32(lane_base + kTS + 64 * chalf, x0);
       tmem_ld32(lane_base + kTS + 64 * chalf + 32, x1);
       tmem_wait_ld();
+      if (i > 0) {  // the state after i full chunks, when a snapshot is due there
+        const int m = snapshot_slot(a, i * kC);
+        if (m >= 0) {
+          float* dst = a.snapshots + (((size_t)n * a.snapshot_slots + m) * H + h) * (kD * kD) +
+                       (size_t)(64 * chalf) * kD + row;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            dst[(size_t)j * kD] = __uint_as_float(x0[j]);
+            dst[(size_t)(32 + j) * kD] = __uint_as_float(x1[j]);
+          }
+        }
+      }
       {
         uint32_t pk[16];
 #pragma unroll
@@ -942,16 +964,21 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
     }
     if (ok && nchunks > 0)
       ok = named_sync_and(kBarState, kChState, mbar_wait(&bar_s, (nchunks - 1) & 1, t.spins));
-    if (ok) {  // final state S^T -> S_T[c][i]
+    if (ok) {  // final state S^T -> S_T[c][i] (and its snapshot slot, if one is due)
       fence_after_sync();
+      const int m = snapshot_slot(a, s1 - s0);
+      float* snap = m >= 0 ? a.snapshots + (((size_t)n * a.snapshot_slots + m) * H + h) * (kD * kD)
+                           : nullptr;
       for (int p = 0; p < 2; ++p) {
         uint32_t r[32];
         const int c0 = 64 * chalf + 32 * p;
         tmem_ld32(lane_base + kTS + c0, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < 32; ++j) {
           a.S_T[sbase + (size_t)(c0 + j) * kD + row] = __uint_as_float(r[j]);
+          if (snap) snap[(size_t)(c0 + j) * kD + row] = __uint_as_float(r[j]);
+        }
       }
     } else if (tid == 0) {
       // a bounded wait gave up: report it, then wait (bounded) for this CTA's

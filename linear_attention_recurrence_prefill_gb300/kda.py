@@ -28,6 +28,9 @@ KDA_F32 = 0
 KDA_BF16 = 1
 
 IMPLS = {"auto": 0, "simt": 1, "tc": 2}
+# KDA_DECAY_*: log_alpha [T, H, d_k] per key channel (KDA), [T, H] per head
+# (Gated DeltaNet), or none (DeltaNet, log_alpha may be None)
+DECAY_MODES = {"channel": 0, "head": 1, "none": 2}
 
 
 class kda_options(ctypes.Structure):
@@ -49,6 +52,9 @@ class kda_options(ctypes.Structure):
         ("debug_timeout", ctypes.c_int),
         ("timeout_spins", ctypes.c_longlong),
         ("phase_events", ctypes.c_void_p),
+        ("decay_mode", ctypes.c_int),
+        ("snapshot_every", ctypes.c_int),
+        ("snapshots", ctypes.c_void_p),
     ]
 
 
@@ -120,6 +126,8 @@ def kda_options_init(**overrides) -> kda_options:
     for key, val in overrides.items():
         if key == "impl" and isinstance(val, str):
             val = IMPLS[val]
+        if key == "decay_mode" and isinstance(val, str):
+            val = DECAY_MODES[val]
         setattr(opt, key, val)
     return opt
 
@@ -163,8 +171,9 @@ def _check_cuda(*ts):
 
 def _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
           eps_norm, workspace, workspace_bytes, max_seqlen, impl, debug_timeout,
-          timeout_spins) -> kda_options:
+          timeout_spins, decay_mode="channel") -> kda_options:
     return kda_options_init(
+        decay_mode=decay_mode,
         chunk=int(chunk), l2norm_qk=int(bool(l2norm_qk)), beta_is_logit=int(bool(beta_is_logit)),
         g_min=float(g_min), q_scale=float(q_scale), eps_l2=float(eps_l2),
         eps_norm=float(eps_norm), gate=_ptr(gate), norm_weight=_ptr(norm_weight),
@@ -196,12 +205,19 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
                 l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
                 q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
                 workspace=None, max_seqlen: int = 0, impl="auto", debug_timeout: bool = False,
-                timeout_spins: int = 0, phase_events=None, stream=None):
+                timeout_spins: int = 0, phase_events=None, decay_mode="channel",
+                snapshot_every: int = 0, snapshots=None, stream=None):
     """Chunked prefill (C ``kda_prefill``).
 
     q, k, log_alpha [T, H, d_k]; v [T, H, d_v]; beta [T, H]; S0 [N, H, d_k, d_v]
     fp32 or None; cu_seqlens [N+1] int32 (device) or None.  Returns (o, S_T);
     o holds y = RMSNorm(o) * w * sigmoid(gate) when ``gate`` is given.
+    ``decay_mode`` "head" takes log_alpha [T, H]; "none" ignores it (None is fine).
+    With ``snapshot_every`` (a multiple of 64) it returns (o, S_T, snapshots),
+    snapshots [N, L // snapshot_every, H, d_k, d_v] fp32 with L = max_seqlen
+    (T // N without cu_seqlens, T with them): slot m holds the state after
+    (m + 1) * snapshot_every tokens of the sequence (zeros, or the given
+    buffer's contents, past its length).
     """
     import torch
     _check_cuda(q, k, v, log_alpha, beta, S0, cu_seqlens, gate, norm_weight, o, S_T)
@@ -217,13 +233,22 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
         S_T = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
     impl_code = IMPLS[impl] if isinstance(impl, str) else int(impl)
     opt = _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
-                eps_norm, None, 0, max_seqlen, impl_code, debug_timeout, timeout_spins)
+                eps_norm, None, 0, max_seqlen, impl_code, debug_timeout, timeout_spins,
+                decay_mode)
     if phase_events is not None:  # list of torch.cuda.Event, (launches + 1) of them
         if any(not e.cuda_event for e in phase_events):
             raise ValueError("phase_events: record each event once first (torch creates "
                              "the CUDA event lazily)")
         ev_arr = (ctypes.c_void_p * len(phase_events))(*[e.cuda_event for e in phase_events])
         opt.phase_events = ctypes.cast(ev_arr, ctypes.c_void_p)
+    if snapshot_every:
+        L = max_seqlen if max_seqlen > 0 else (T if cu_seqlens is not None else T // N)
+        if snapshots is None:
+            snapshots = torch.zeros((N, L // snapshot_every, H, d_k, d_v), dtype=torch.float32,
+                                    device=q.device)
+        _check_cuda(snapshots)
+        opt.snapshot_every = int(snapshot_every)
+        opt.snapshots = _ptr(snapshots)
     need = kda_prefill_workspace_size(T, N, H, d_k, d_v, opt)
     if need > 0:
         if workspace is None:
@@ -235,15 +260,17 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
                             ctypes.byref(opt), _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_prefill")
+    if snapshot_every:
+        return o, S_T, snapshots
     return o, S_T
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weight=None,
                     l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
                     q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
-                    stream=None):
+                    decay_mode="channel", stream=None):
     """One decode step (C ``kda_decode_step``); S [N, H, d_k, d_v] is updated in place.
-    Returns o [N, H, d_v]."""
+    Returns o [N, H, d_v].  log_alpha is [N, H] with decay_mode "head"."""
     import torch
     _check_cuda(q, k, v, log_alpha, beta, S, o, gate, norm_weight)
     N, H, d_k = q.shape
@@ -251,7 +278,7 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weig
     if o is None:
         o = torch.empty((N, H, d_v), dtype=q.dtype, device=q.device)
     opt = _opts(gate, norm_weight, 0, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
-                eps_norm, None, 0, 0, 0, False, 0)
+                eps_norm, None, 0, 0, 0, False, 0, decay_mode)
     rc = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                 _ptr(S), _ptr(o), N, H, d_k, d_v, _dtype_code(q),
                                 ctypes.byref(opt), _stream(stream))
@@ -287,7 +314,7 @@ def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: i
                         o=None, S_T=None, *, gate=None, norm_weight=None, l2norm_qk: bool = True,
                         beta_is_logit: bool = False, g_min: float = -5.0, q_scale: float = 1.0,
                         eps_l2: float = 1e-6, eps_norm: float = 1e-6, max_seqlen: int = 0,
-                        stream=None):
+                        decay_mode="channel", stream=None):
     """Prefill with the library's built-in scratch (C ``kda_prefill_noalloc``).
 
     For callers that must not allocate device memory: the library allocates
@@ -306,7 +333,7 @@ def kda_prefill_noalloc(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: i
     if S_T is None:
         S_T = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
     opt = _opts(gate, norm_weight, 64, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
-                eps_norm, None, 0, max_seqlen, IMPLS["tc"], False, 0)
+                eps_norm, None, 0, max_seqlen, IMPLS["tc"], False, 0, decay_mode)
     rc = load().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                     _ptr(S0), _ptr(cu_seqlens), N, _ptr(o), _ptr(S_T), T, H, d_k,
                                     d_v, _dtype_code(q), ctypes.byref(opt), _stream(stream))

@@ -40,10 +40,12 @@ def test_options_defaults():
     assert o.g_min == -5.0 and o.q_scale == 1.0
     assert abs(o.eps_l2 - 1e-6) < 1e-12 and abs(o.eps_norm - 1e-6) < 1e-12
     assert not o.gate and not o.workspace and o.workspace_bytes == 0
+    assert o.decay_mode == kda.DECAY_MODES["channel"] == 0
+    assert o.snapshot_every == 0 and not o.snapshots
     # layout of struct kda_options on LP64 (7 x 4-byte fields, 3 pointers,
-    # size_t, 3 ints, padding, long long, pointer)
-    assert ctypes.sizeof(kda.kda_options) == 96
-    assert kda.kda_abi_version() == 1
+    # size_t, 3 ints, padding, long long, pointer, 2 ints, pointer)
+    assert ctypes.sizeof(kda.kda_options) == 112
+    assert kda.kda_abi_version() == 2
 
 
 def test_status_strings():
@@ -102,9 +104,34 @@ def test_prefill_rejects(kw, code):
     (dict(max_seqlen=1000), kda.KDA_ERR_SHAPE),
     (dict(impl=9), kda.KDA_ERR_UNSUPPORTED),
     (dict(gate=A + 2), kda.KDA_ERR_ALIGN),
+    (dict(decay_mode=3), kda.KDA_ERR_ARG),
+    (dict(decay_mode=-1), kda.KDA_ERR_ARG),
+    (dict(snapshot_every=32, snapshots=A), kda.KDA_ERR_ARG),
+    (dict(snapshot_every=-64, snapshots=A), kda.KDA_ERR_ARG),
+    (dict(snapshot_every=64), kda.KDA_ERR_ARG),
+    (dict(snapshot_every=64, snapshots=A + 4), kda.KDA_ERR_ALIGN),
 ])
 def test_prefill_rejects_options(opt_kw, code):
     assert _prefill(opt=kda.kda_options_init(**opt_kw)) == code
+
+
+@no_gpu
+def test_log_alpha_requirements_follow_the_decay_mode():
+    # per channel: required and 16-byte aligned; per head: 4-byte alignment
+    assert _prefill(la=None) == kda.KDA_ERR_ARG
+    assert _prefill(la=A + 4) == kda.KDA_ERR_ALIGN
+    assert _prefill(la=None, opt=kda.kda_options_init(decay_mode="head")) == kda.KDA_ERR_ARG
+    assert _prefill(la=A + 2, opt=kda.kda_options_init(decay_mode="head")) == kda.KDA_ERR_ALIGN
+    # a 4-byte aligned per-head array, and no array without decay, pass the
+    # pointer and alignment checks: the option check that follows them (a floor
+    # below -5) is what stops these calls, before anything could launch
+    assert _prefill(la=A + 4, opt=kda.kda_options_init(decay_mode="head", g_min=-6.0)) == \
+        kda.KDA_ERR_ARG
+    assert _prefill(la=A + 4, opt=kda.kda_options_init(g_min=-6.0)) == kda.KDA_ERR_ALIGN
+    assert _prefill(la=None, opt=kda.kda_options_init(decay_mode="none", g_min=-6.0)) == \
+        kda.KDA_ERR_ARG
+    assert _prefill(la=None, dtype=7, opt=kda.kda_options_init(decay_mode="none")) == \
+        kda.KDA_ERR_DTYPE
 
 
 @no_gpu
