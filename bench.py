@@ -56,9 +56,10 @@ def prefill_flops(chunk: int, T_=T, H_=H, d=D):
 # DRAM bytes (read + write) per launch from an ncu capture of the kernel as it
 # stands (profiles/ holds the summaries); None until captured after a change.
 TRAFFIC: dict[str, float | None] = {
-    # profiles/prefill_tc_kernels_k3.md (dram read + write of one launch)
-    "prep_kernel": None,  # changed since the last capture
-    "chain_kernel": None,  # changed since the last capture
+    # profiles/prep_kernel_k3_prefill.md, profiles/chain_kernel_k3_prefill.md
+    # (dram read + write of one launch)
+    "prep_kernel": 504.567808e6 + 406.384384e6,
+    "chain_kernel": 563.148288e6 + 87.531008e6,
     # profiles/decode_kernel_k3_decode.md
     "decode_kernel<128,bf16>": 754.506752e6,
 }
@@ -348,7 +349,19 @@ def run_decode(args, dev, stream, dist, peaks):
         for t in range(n):
             kda.kda_decode_step(di.q[t], di.k[t], di.v[t], di.log_alpha[t], di.beta[t], S, o)
 
-    steps(8)
+    # The 256-step loop runs as one captured CUDA graph, as a serving loop
+    # would: the launches are recorded once, so the timed region is the GPU's
+    # work, not the per-call Python marshalling.
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        steps(8)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        steps(DEC_STEPS)
+    graph.replay()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(1, min(args.steps, 3))
@@ -356,13 +369,14 @@ def run_decode(args, dev, stream, dist, peaks):
     for _ in range(reps):
         barrier(dist)
         torch.cuda.synchronize()
-        ev0.record(stream)
-        steps(DEC_STEPS)
-        ev1.record(stream)
+        ev0.record()
+        graph.replay()
+        ev1.record()
         torch.cuda.synchronize()
         times.append(ev0.elapsed_time(ev1))
     ms = max_over_ranks(dist, statistics.median(times))
     per_step_ms = ms / DEC_STEPS
+    del graph
     bytes_step = DEC_BYTES_PER_UNIT * DEC_N * H
     gbs = bytes_step / (per_step_ms / 1e3) / 1e9
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -265,6 +265,9 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
     return o, S_T
 
 
+_DECODE_OPTS: dict = {}
+
+
 def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weight=None,
                     l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
                     q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
@@ -277,8 +280,17 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weig
     d_v = v.shape[2]
     if o is None:
         o = torch.empty((N, H, d_v), dtype=q.dtype, device=q.device)
-    opt = _opts(gate, norm_weight, 0, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
-                eps_norm, None, 0, 0, 0, False, 0, decay_mode)
+    # a decode loop calls this once per token: the options struct is built once
+    # per distinct setting
+    key = (_ptr(gate), _ptr(norm_weight), bool(l2norm_qk), bool(beta_is_logit), float(g_min),
+           float(q_scale), float(eps_l2), float(eps_norm), decay_mode)
+    opt = _DECODE_OPTS.get(key)
+    if opt is None:
+        opt = _opts(gate, norm_weight, 0, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+                    eps_norm, None, 0, 0, 0, False, 0, decay_mode)
+        if len(_DECODE_OPTS) > 64:
+            _DECODE_OPTS.clear()
+        _DECODE_OPTS[key] = opt
     rc = load().kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
                                 _ptr(S), _ptr(o), N, H, d_k, d_v, _dtype_code(q),
                                 ctypes.byref(opt), _stream(stream))
