@@ -76,11 +76,11 @@ struct DecodeArgs {
 
 // log alpha of token-head row `row` (token * H + head), key channel c, under
 // the decay mode (KDA_DECAY_*), before the floor.
+// Written without branches so that the load issues with the token's others.
 __device__ __forceinline__ float log_alpha_at(const float* la, int mode, size_t row, int d,
                                               int c) {
-  if (mode == KDA_DECAY_CHANNEL) return la[row * d + c];
-  if (mode == KDA_DECAY_HEAD) return la[row];
-  return 0.f;
+  const size_t off = mode == KDA_DECAY_CHANNEL ? row * d + c : row;
+  return mode == KDA_DECAY_NONE ? 0.f : la[off];
 }
 
 // Token range [t0, t1) of sequence n.

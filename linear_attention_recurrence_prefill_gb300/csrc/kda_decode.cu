@@ -45,13 +45,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
   const T* k = static_cast<const T*>(a.k);
   const T* v = static_cast<const T*>(a.v);
   const size_t base = (size_t)unit * D;
+  // every global load of the token (and beta) is issued before the first barrier
+  float qv = 0.f, kv = 0.f, vv = 0.f, lav = 0.f, bv = 0.f;
   if (tid < D) {
-    sq[tid] = to_f32(q[base + tid]);
-    sk[tid] = to_f32(k[base + tid]);
-    sv[tid] = to_f32(v[base + tid]);
-    const float la =
-        fminf(fmaxf(log_alpha_at(a.log_alpha, a.decay_mode, (size_t)unit, D, tid), a.g_min), 0.f);
-    sa[tid] = expf(la);
+    qv = to_f32(q[base + tid]);
+    kv = to_f32(k[base + tid]);
+    vv = to_f32(v[base + tid]);
+    lav = log_alpha_at(a.log_alpha, a.decay_mode, (size_t)unit, D, tid);
+  }
+  if (tid == 0) bv = to_f32(static_cast<const T*>(a.beta)[unit]);
+  if (tid < D) {
+    sq[tid] = qv;
+    sk[tid] = kv;
+    sv[tid] = vv;
+    sa[tid] = expf(fminf(fmaxf(lav, a.g_min), 0.f));
   }
   __syncthreads();
   if (tid < 32) {
@@ -65,7 +72,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
     ssk = warp_sum(ssk);
     skq = warp_sum(skq);
     if (tid == 0) {
-      float b = to_f32(static_cast<const T*>(a.beta)[unit]);
+      float b = bv;
       if (a.beta_is_logit) b = sigmoidf_(b);
       float iq = 1.f, ik = 1.f;
       if (a.l2norm_qk) {
