@@ -291,29 +291,27 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   //      256 B and log alpha rows of 512 B; rows past the sequence end are
   //      zero-filled (an identity step).  With one decay per head (or none) the
   //      decay rows are filled by broadcasting the row's value instead ----
-  const int n_copy = a.decay_mode == KDA_DECAY_CHANNEL ? kC * 64 : kC * 32;
-  for (int e = tid; e < n_copy; e += kPrepThreads) {
-    const int reg = e >> 10, w = e & 1023;  // 0: q, 1: k, 2-3: log alpha
-    int r, col16;
-    uint32_t dst;
-    const char* src;
-    if (reg < 2) {
-      r = w >> 4;
-      col16 = w & 15;
-      dst = smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + col16 * 16);
-      src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q);
-    } else {
-      const int w2 = e - 2048;
-      r = w2 >> 5;
-      col16 = w2 & 31;
-      // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
-      dst = smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + (col16 >> 1) * 16);
-      src = reinterpret_cast<const char*>(a.log_alpha);
-    }
+  // q, k rows: 16-byte chunk e of row e / 16 (1024 chunks each)
+#pragma unroll 4
+  for (int e = tid; e < kC * 32; e += kPrepThreads) {
+    const int reg = e >> 10, w = e & 1023, r = w >> 4, col16 = w & 15;
     const int rr = r < len ? r : 0;
-    const size_t row = (size_t)(tok0 + rr) * H + h;
-    src += row * (reg < 2 ? 256 : 512) + (size_t)col16 * 16;
-    cp_async16(dst, src, r < len ? 16u : 0u);
+    const char* src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q) +
+                      ((size_t)(tok0 + rr) * H + h) * 256 + (size_t)col16 * 16;
+    cp_async16(smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + col16 * 16), src,
+               r < len ? 16u : 0u);
+  }
+  if (a.decay_mode == KDA_DECAY_CHANNEL) {  // log alpha rows of 512 B
+#pragma unroll 4
+    for (int e = tid; e < kC * 32; e += kPrepThreads) {
+      const int r = e >> 5, col16 = e & 31;
+      const int rr = r < len ? r : 0;
+      const char* src = reinterpret_cast<const char*>(a.log_alpha) +
+                        ((size_t)(tok0 + rr) * H + h) * 512 + (size_t)col16 * 16;
+      // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
+      cp_async16(smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + (col16 >> 1) * 16), src,
+                 r < len ? 16u : 0u);
+    }
   }
   cp_async_commit();
   if (a.decay_mode != KDA_DECAY_CHANNEL) {
