@@ -61,7 +61,7 @@ TRAFFIC: dict[str, float | None] = {
     "prep_kernel": 504.567808e6 + 406.384384e6,
     "chain_kernel": 563.148288e6 + 87.531008e6,
     # profiles/decode_kernel_k3_decode.md
-    "decode_kernel<128,bf16>": 754.506752e6,
+    "decode_kernel<128,bf16>": 410.566656e6 + 343.659776e6,
 }
 
 
