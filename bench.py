@@ -193,6 +193,9 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
+N_UP = 4  # host->device copy streams of the end-to-end leg
+
+
 def run_ours(args, rank, world, local, dist):
     import torch
 
@@ -260,35 +263,79 @@ def run_ours(args, rank, world, local, dist):
     dom_ms = kern_ms[dom]
 
     # --- end to end through the public API with host buffers ---
+    # A serving loop pipelines steps: step i+1's inputs go up (two copy
+    # streams, double-buffered device inputs and outputs) while step i runs,
+    # and step i's results come back on a third stream.  Every step's own
+    # host->device and device->host copies are inside the timed region.
     host = {n: getattr(inp, n).cpu().pin_memory() for n in
             ("q", "k", "v", "log_alpha", "beta", "gate", "S0")}
-    devb = {n: torch.empty_like(getattr(inp, n)) for n in host}
+    devb = [{n: torch.empty_like(getattr(inp, n)) for n in host} for _ in range(2)]
+    outs = [(torch.empty_like(o), torch.empty_like(S_T)) for _ in range(2)]
     y_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     st_host = torch.empty(S_T.shape, dtype=S_T.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = y_host.numel() * y_host.element_size() + st_host.numel() * st_host.element_size()
+    # copies in flight on four streams: each tensor in two halves, the pieces
+    # dealt out largest first
+    up = [torch.cuda.Stream() for _ in range(N_UP)]
+    down = torch.cuda.Stream()
+    pieces = []
+    for n, t in host.items():
+        half = (t.shape[0] + 1) // 2
+        pieces += [(n, 0, half), (n, half, t.shape[0])]
+    pieces.sort(key=lambda p: -(p[2] - p[1]) * host[p[0]][0].numel() * host[p[0]].element_size())
+    groups = [[] for _ in up]
+    load = [0] * len(up)
+    for pc in pieces:
+        g = load.index(min(load))
+        groups[g].append(pc)
+        load[g] += (pc[2] - pc[1]) * host[pc[0]][0].numel() * host[pc[0]].element_size()
+    done_in = [[torch.cuda.Event() for _ in up] for _ in range(2)]
+    done_run = [torch.cuda.Event() for _ in range(2)]
+    done_out = [torch.cuda.Event() for _ in range(2)]
+    started = [False, False]
 
-    def e2e_step():
-        for n, t in host.items():
-            devb[n].copy_(t, non_blocking=True)
-        kda.kda_prefill(devb["q"], devb["k"], devb["v"], devb["log_alpha"], devb["beta"],
-                        devb["S0"], None, 1, o, S_T, gate=devb["gate"], impl=args.path,
-                        workspace=ws if ws_bytes else None)
-        y_host.copy_(o, non_blocking=True)
-        st_host.copy_(S_T, non_blocking=True)
+    def e2e_step(i):
+        b = i % 2
+        for g, grp in enumerate(groups):
+            if started[b]:                      # the buffer's previous step has run
+                up[g].wait_event(done_run[b])
+            with torch.cuda.stream(up[g]):
+                for n, r0, r1 in grp:
+                    devb[b][n][r0:r1].copy_(host[n][r0:r1], non_blocking=True)
+            done_in[b][g].record(up[g])
+        for ev in done_in[b]:
+            stream.wait_event(ev)
+        if started[b]:                          # its outputs have been read back
+            stream.wait_event(done_out[b])
+        ob, sb = outs[b]
+        d = devb[b]
+        kda.kda_prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["S0"], None, 1,
+                        ob, sb, gate=d["gate"], impl=args.path,
+                        workspace=ws if ws_bytes else None, stream=stream)
+        done_run[b].record(stream)
+        down.wait_event(done_run[b])
+        with torch.cuda.stream(down):
+            y_host.copy_(ob, non_blocking=True)
+            st_host.copy_(sb, non_blocking=True)
+        done_out[b].record(down)
+        started[b] = True
 
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        e2e_step()
+    e2e_steps = max(4, min(args.steps, 10))
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(dist)
     ev0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    for st in up + [down]:
+        st.wait_stream(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_stream(down)
     ev1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / e2e_steps)
-    del host, devb
+    del host, devb, outs
 
     # --- decode (state in place; 805 MB of state > L2) ---
     dec = run_decode(args, dev, stream, dist, peaks)
