@@ -72,6 +72,9 @@ __constant__ uint32_t kWsPartOff[kWsParts] = {kWsUt, kWsWQ, kWsKh, kWsP, kWsGam}
 __constant__ uint32_t kWsPartLen[kWsParts] = {16384, 32768, 16384, 8192, 512};
 
 constexpr uint32_t kIdF16Bf16 = idesc_f16(128, 16, true);   // Gram: M128 N16 bf16
+constexpr uint32_t kIdGram32 = idesc_f16(128, 32, true);    // Gram: M128 N32 bf16
+// TMEM columns of the Gram per column tile b: [hi.hi | hi.lo | lo.hi], 16 each
+constexpr uint32_t kGramCols = 48;
 constexpr uint32_t kIdF16N64 = idesc_f16(128, 64, false);   // fp16, N = 64
 constexpr uint32_t kIdF16N128 = idesc_f16(128, 128, false); // fp16, N = 128
 constexpr uint32_t kIdKh = idesc_f16(128, 128, false, false, true);  // fp16, N = 128, B MN-major
@@ -156,6 +159,8 @@ __device__ __forceinline__ int find_seq(const int* base, int N, int gid) {
 // thread, so that two CTAs share an SM and hide each other's waits.
 // Shared memory (offsets from a 1024-aligned base):
 constexpr int kPrepThreads = 256;
+constexpr int kPrepHalf = 128;                   // threads per warp group (steps 5 / 6)
+constexpr uint32_t kBarRow = 1, kBarSolve = 2;   // their named barriers
 constexpr uint32_t kPrepQ = 0;            // q rows, bf16 [64][128] (256 B rows)
 constexpr uint32_t kPrepK = 16384;        // k rows, bf16 [64][128]
 constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
@@ -175,12 +180,14 @@ constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
 // TMEM: Gram D in columns 0..63, then U~^T (64 columns) and W (128 columns)
 constexpr uint32_t kPrepTmemCols = 256, kTdU = 0, kTdW = 64;
+static_assert(4 * kGramCols <= kPrepTmemCols, "Gram accumulators fit the TMEM allocation");
 constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
 static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
 static_assert(kPrepBlo + 2048 <= kPrepSmall, "Gram operands inside the reused region");
+static_assert(kPrepBlo == kPrepBhi + 2048, "B_lo is rows 16..31 of the N = 32 Gram operand");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
 static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
               "float4 access to the inverse and the scratch");
@@ -468,19 +475,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     if (!ok) goto fail;
     if (tid == 0) {
       fence_after_sync();
-      const uint32_t d = tmem + 16 * b;
+      // A_hi against [B_hi; B_lo] (one N = 32 product: the B_lo tile follows the
+      // B_hi tile as its rows 16..31) and A_lo against B_hi: A is read twice per
+      // K-step instead of three times
+      const uint32_t d = tmem + kGramCols * b;
       const uint32_t ahi = smem_u32(sm + kPrepAhi), alo = smem_u32(sm + kPrepAlo);
-      const uint32_t bhi = smem_u32(sm + kPrepBhi), blo = smem_u32(sm + kPrepBlo);
+      const uint32_t bhi = smem_u32(sm + kPrepBhi);
       const uint64_t dahi = desc_k_sw128(ahi, 0), dalo = desc_k_sw128(alo, 0);
-      const uint64_t dbhi = desc_k_sw128(bhi, 0), dblo = desc_k_sw128(blo, 0);
+      const uint64_t dbhi = desc_k_sw128(bhi, 0);
       // a K-step of 16 elements is 32 bytes: +2 in the descriptor's address field
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(d, dahi + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, (kh | ks) ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) mma_ss(d, dahi + 2 * ks, dblo + 2 * ks, kIdF16Bf16, 1u);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) mma_ss(d, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, 1u);
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t acc = (kh | ks) ? 1u : 0u;
+        mma_ss(d, dahi + 2 * ks, dbhi + 2 * ks, kIdGram32, acc);
+        mma_ss(d + 32, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, acc);
+      }
       mma_commit(&bar_mma);
     }
   }
@@ -495,9 +504,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     {
       const int quarter = warp & 3, chalf = warp >> 2;
       const int r = quarter * 32 + lane;
-      uint32_t x[32];
-      tmem_ld32(taddr(tmem, quarter * 32, 32 * chalf), x);
-      tmem_wait_ld();
+      uint32_t x[32];  // columns j = 32 chalf .. +31: tiles 2 chalf, 2 chalf + 1
+#pragma unroll
+      for (int t2 = 0; t2 < 2; ++t2) {
+        uint32_t y[32], z[16];
+        const uint32_t col = kGramCols * (2 * chalf + t2);
+        tmem_ld32(taddr(tmem, quarter * 32, col), y);       // hi.hi | hi.lo
+        tmem_ld16(taddr(tmem, quarter * 32, col + 32), z);  // lo.hi
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          x[16 * t2 + j] = __float_as_uint(__uint_as_float(y[j]) + __uint_as_float(y[16 + j]) +
+                                           __uint_as_float(z[j]));
+      }
       if (r < kC) {
         const float br = s_beta[r];
 #pragma unroll
@@ -524,17 +543,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     fence_before_sync();
     __syncthreads();
 
-    // ---- 5. row pass: -Q~ rows, K^ rows and G_C straight to the workspace, K~
-    //      (fp16) into the MN-major operand over the k rows; then the v rows, by
-    //      16-byte asynchronous copies (bf16, landing during the solve), into the
-    //      MN-major operand over the q rows.  Row item (row r, 8-channel group
-    //      c16) = tid + 256 m ----
-    uint4 ktl[4];
-    {
+    // ---- 5 / 6. Two warp groups in parallel (disjoint data, named barriers):
+    //      warps 4-7 run the row pass, warps 0-3 invert (I + A) ----
+    float* X = reinterpret_cast<float*>(sm + kPrepInv);
+    float* Y = reinterpret_cast<float*>(sm + kPrepY);
+    if (tid >= kPrepHalf) {
+      // ---- 5. row pass: -Q~ rows, K^ rows and G_C straight to the workspace, K~
+      //      (fp16) into the MN-major operand over the k rows; then the v rows, by
+      //      16-byte asynchronous copies (bf16, landing during the solve), into
+      //      the MN-major operand over the q rows.  Row item (row r, 8-channel
+      //      group c16) = rt + 128 m ----
+      const int rt = tid - kPrepHalf;
+      uint4 ktl[8];
       const float* Gl = G + (kC - 1) * kD;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
+      for (int m = 0; m < 8; ++m) {
+        const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
         float g8[8], gl8[8], kf[8], qf[8];
         ld8g(G + r * kD, c16, g8);
         ld8g(Gl, c16, gl8);
@@ -562,85 +586,85 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
             make_uint4(wh[0], wh[1], wh[2], wh[3]);
       }
-      if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(Gl[gpos(tid)]);
-    }
-    __syncthreads();  // every read of the q and k rows is done: their space takes K~ and V
+      reinterpret_cast<float*>(ws + kWsGam)[rt] = ex2f(Gl[gpos(rt)]);
+      named_sync(kBarRow, kPrepHalf);  // every read of the q, k rows is done: they take K~, V
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15;
-      *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = ktl[m];
-      const int rr = r < len ? r : 0;
-      cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
-                 v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
-    }
-    cp_async_commit();
-
-    // ---- 6. X = (I + A)^-1 by 16 x 16 blocks ----
-    float* X = reinterpret_cast<float*>(sm + kPrepInv);
-    float* Y = reinterpret_cast<float*>(sm + kPrepY);
-    if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
-      const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update rows
-      float x[16];                                          // below: a 15-FMA chain)
-#pragma unroll
-      for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-      for (int m = 0; m < 15; ++m) {
-#pragma unroll
-        for (int r = m + 1; r < 16; ++r) x[r] -= Amat[(o + r) * kAs + o + m] * x[m];
+      for (int m = 0; m < 8; ++m) {
+        const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15;
+        *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = ktl[m];
+        const int rr = r < len ? r : 0;
+        cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
+                   v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
       }
+      cp_async_commit();
+    } else {
+      // ---- 6. X = (I + A)^-1 by 16 x 16 blocks ----
+      if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
+        const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update
+        float x[16];                                          // rows below: 15-FMA chain)
 #pragma unroll
-      for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
-    } else {  // the blocks above the diagonal are zero
-      for (int e = tid - 64; e < 6 * 256; e += kPrepThreads - 64) {
-        const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
-      }
-    }
-    __syncthreads();
-    // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj.
-    // The sum is split by 16-token tile p of m: one unrolled 16-term product per
-    // thread (4 adjacent columns of one row, float4 loads), partial sums in Y.
+        for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-    for (int dd = 1; dd < 4; ++dd) {
-      const int nblk = 4 - dd;
-      if (tid < nblk * dd * 64) {
-        const int p = tid / (nblk * 64), rem = tid - p * (nblk * 64);
-        const int bj = rem >> 6, bi = bj + dd, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
-        const int m0 = 16 * (bj + p);
-        const float* arow = Amat + (16 * bi + r) * kAs + m0;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m = 0; m < 15; ++m) {
 #pragma unroll
-        for (int mm = 0; mm < 16; ++mm) {
-          const float am = arow[mm];
-          const float4 x4 = *reinterpret_cast<const float4*>(X + (m0 + mm) * kXs + 16 * bj + c4);
-          acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+          for (int r = m + 1; r < 16; ++r) x[r] -= Amat[(o + r) * kAs + o + m] * x[m];
         }
-        *reinterpret_cast<float4*>(Y + ((p * nblk + bj) << 8) + r * 16 + c4) = acc;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
+      } else {  // the blocks above the diagonal are zero
+        for (int e = tid - 64; e < 6 * 256; e += kPrepHalf - 64) {
+          const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+          const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+          const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+          X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
+        }
       }
-      __syncthreads();
-      if (tid < nblk * 64) {
-        const int bj = tid >> 6, bi = bj + dd, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
+      named_sync(kBarSolve, kPrepHalf);
+      // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj.
+      // The sum is split by 16-token tile p of m: unrolled 16-term products (4
+      // adjacent columns of one row, float4 loads), partial sums in Y.
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float xm = xrow[m];
-          float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
+      for (int dd = 1; dd < 4; ++dd) {
+        const int nblk = 4 - dd;
+        for (int u = tid; u < nblk * dd * 64; u += kPrepHalf) {
+          const int p = u / (nblk * 64), rem = u - p * (nblk * 64);
+          const int bj = rem >> 6, bi = bj + dd, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
+          const int m0 = 16 * (bj + p);
+          const float* arow = Amat + (16 * bi + r) * kAs + m0;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int pp = 1; pp < dd; ++pp) {
-            const float4 z4 =
-                *reinterpret_cast<const float4*>(Y + ((pp * nblk + bj) << 8) + m * 16 + c4);
-            y4.x += z4.x; y4.y += z4.y; y4.z += z4.z; y4.w += z4.w;
+          for (int mm = 0; mm < 16; ++mm) {
+            const float am = arow[mm];
+            const float4 x4 =
+                *reinterpret_cast<const float4*>(X + (m0 + mm) * kXs + 16 * bj + c4);
+            acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
           }
-          acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
+          *reinterpret_cast<float4*>(Y + ((p * nblk + bj) << 8) + r * 16 + c4) = acc;
         }
-        *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        named_sync(kBarSolve, kPrepHalf);
+        for (int u = tid; u < nblk * 64; u += kPrepHalf) {
+          const int bj = u >> 6, bi = bj + dd, r = (u >> 2) & 15, c4 = (u & 3) * 4;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const float xm = xrow[m];
+            float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
+#pragma unroll
+            for (int pp = 1; pp < dd; ++pp) {
+              const float4 z4 =
+                  *reinterpret_cast<const float4*>(Y + ((pp * nblk + bj) << 8) + m * 16 + c4);
+              y4.x += z4.x; y4.y += z4.y; y4.z += z4.z; y4.w += z4.w;
+            }
+            acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
+          }
+          *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
+              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        named_sync(kBarSolve, kPrepHalf);
       }
-      __syncthreads();
     }
+    __syncthreads();  // X, the workspace rows, K~ and the v copies are all issued
 
     // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
     //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
