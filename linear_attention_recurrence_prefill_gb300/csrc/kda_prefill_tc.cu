@@ -179,8 +179,9 @@ constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 //   T as bf16 hi/lo K-major [64 (t)][64 (j)] tiles over the decay rows
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
 // TMEM: Gram D in columns 0..63, then U~^T (64 columns) and W (128 columns)
-constexpr uint32_t kPrepTmemCols = 256, kTdU = 0, kTdW = 64;
+constexpr uint32_t kPrepTmemCols = 256, kTdU = 0, kTdW = 64, kTdScratch = 192;
 static_assert(4 * kGramCols <= kPrepTmemCols, "Gram accumulators fit the TMEM allocation");
+static_assert(kTdW + 128 <= kTdScratch && kTdScratch + 32 <= kPrepTmemCols, "TMEM scratch");
 constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
@@ -258,20 +259,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PrefillArgs& a = t.a;
 
-  // ---- which chunk ----
-  const int gid = blockIdx.x, h = blockIdx.y;
+  // ---- work items: (chunk, head) pairs, item w = h * total + gid; a CTA takes
+  //      items blockIdx.x, + gridDim.x, ... and streams the next item's inputs
+  //      into its buffers while it writes out the current one ----
   const int total = t.chunk_base[a.N];
-  if (gid >= total) return;
-  const int n = find_seq(t.chunk_base, a.N, gid);
-  const int c = gid - t.chunk_base[n];
-  int s0, s1;
-  seq_range(a.cu_seqlens, a.N, a.T_total, n, s0, s1);
-  const int tok0 = s0 + c * kC;
-  const int len = min(kC, s1 - tok0);
-  if (len <= 0) return;
+  const int items = total * a.H;
+  if ((int)blockIdx.x >= items) return;
   const size_t H = (size_t)a.H;
-  uint8_t* ws = ws_block(t, gid, h);
-
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
   const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
   const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
@@ -294,458 +288,497 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   fence_after_sync();
   const uint32_t tmem = tmem_base;
 
-  // ---- 1. input rows by 16-byte asynchronous copies (all threads): q, k rows of
-  //      256 B and log alpha rows of 512 B; rows past the sequence end are
-  //      zero-filled (an identity step).  With one decay per head (or none) the
-  //      decay rows are filled by broadcasting the row's value instead ----
-  // q, k rows: 16-byte chunk e of row e / 16 (1024 chunks each)
-#pragma unroll 4
-  for (int e = tid; e < kC * 32; e += kPrepThreads) {
-    const int reg = e >> 10, w = e & 1023, r = w >> 4, col16 = w & 15;
-    const int rr = r < len ? r : 0;
-    const char* src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q) +
-                      ((size_t)(tok0 + rr) * H + h) * 256 + (size_t)col16 * 16;
-    cp_async16(smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + col16 * 16), src,
-               r < len ? 16u : 0u);
-  }
-  if (a.decay_mode == KDA_DECAY_CHANNEL) {  // log alpha rows of 512 B
+  auto decode = [&](int wi, int& gid_, int& h_, int& tok0_, int& len_) {
+    h_ = wi / total;
+    gid_ = wi - h_ * total;
+    const int n_ = find_seq(t.chunk_base, a.N, gid_);
+    int s0_, s1_;
+    seq_range(a.cu_seqlens, a.N, a.T_total, n_, s0_, s1_);
+    tok0_ = s0_ + (gid_ - t.chunk_base[n_]) * kC;
+    len_ = min(kC, s1_ - tok0_);
+  };
+  auto issue_inputs = [&](int h, int tok0, int len) {
+    // ---- 1. input rows by 16-byte asynchronous copies (all threads): q, k rows of
+    //      256 B and log alpha rows of 512 B; rows past the sequence end are
+    //      zero-filled (an identity step).  With one decay per head (or none) the
+    //      decay rows are filled by broadcasting the row's value instead ----
+    // q, k rows: 16-byte chunk e of row e / 16 (1024 chunks each)
 #pragma unroll 4
     for (int e = tid; e < kC * 32; e += kPrepThreads) {
-      const int r = e >> 5, col16 = e & 31;
+      const int reg = e >> 10, wd = e & 1023, r = wd >> 4, col16 = wd & 15;
       const int rr = r < len ? r : 0;
-      const char* src = reinterpret_cast<const char*>(a.log_alpha) +
-                        ((size_t)(tok0 + rr) * H + h) * 512 + (size_t)col16 * 16;
-      // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
-      cp_async16(smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + (col16 >> 1) * 16), src,
+      const char* src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q) +
+                        ((size_t)(tok0 + rr) * H + h) * 256 + (size_t)col16 * 16;
+      cp_async16(smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + col16 * 16), src,
                  r < len ? 16u : 0u);
     }
-  }
-  cp_async_commit();
-  if (a.decay_mode != KDA_DECAY_CHANNEL) {
-    for (int e = tid; e < kC * 32; e += kPrepThreads) {  // 16-byte words of the rows
-      const int r = e >> 5, w = e & 31;
-      const float g = (r < len && a.decay_mode == KDA_DECAY_HEAD)
-                          ? a.log_alpha[(size_t)(tok0 + r) * H + h] : 0.f;
-      *reinterpret_cast<float4*>(sm + kPrepG + r * 512 + w * 16) = make_float4(g, g, g, g);
+    if (a.decay_mode == KDA_DECAY_CHANNEL) {  // log alpha rows of 512 B
+#pragma unroll 4
+      for (int e = tid; e < kC * 32; e += kPrepThreads) {
+        const int r = e >> 5, col16 = e & 31;
+        const int rr = r < len ? r : 0;
+        const char* src = reinterpret_cast<const char*>(a.log_alpha) +
+                          ((size_t)(tok0 + rr) * H + h) * 512 + (size_t)col16 * 16;
+        // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
+        cp_async16(smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + (col16 >> 1) * 16), src,
+                   r < len ? 16u : 0u);
+      }
     }
-  }
-  if (tid < kC) {
-    float b = 0.f;
-    if (tid < len) {
-      b = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
-      if (a.beta_is_logit) b = sigmoidf_(b);
+    cp_async_commit();
+    if (a.decay_mode != KDA_DECAY_CHANNEL) {
+      for (int e = tid; e < kC * 32; e += kPrepThreads) {  // 16-byte words of the rows
+        const int r = e >> 5, wd = e & 31;
+        const float g = (r < len && a.decay_mode == KDA_DECAY_HEAD)
+                            ? a.log_alpha[(size_t)(tok0 + r) * H + h] : 0.f;
+        *reinterpret_cast<float4*>(sm + kPrepG + r * 512 + wd * 16) = make_float4(g, g, g, g);
+      }
     }
-    s_beta[tid] = b;
-  }
-  cp_async_wait_all();
+    if (tid < kC) {
+      float b = 0.f;
+      if (tid < len) {
+        b = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
+        if (a.beta_is_logit) b = sigmoidf_(b);
+      }
+      s_beta[tid] = b;
+    }
+  };
+
+  int item = blockIdx.x, gid, h, tok0, len;
+  decode(item, gid, h, tok0, len);
+  issue_inputs(h, tok0, len);
   uint32_t mma_phase = 0;
   bool ok = true;
-  __syncthreads();
+  for (;;) {
+    uint8_t* ws = ws_block(t, gid, h);
+    cp_async_wait_all();
+    __syncthreads();
 
-  // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
-  //      registers); L2 norms of the q, k rows (warps 4-7, four rows at a time) ----
-  if (tid < kD) {  // thread tid scans word tid of the rows (whichever channel it holds)
-    float x[kC];
+    // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
+    //      registers); L2 norms of the q, k rows (warps 4-7, four rows at a time) ----
+    if (tid < kD) {  // thread tid scans word tid of the rows (whichever channel it holds)
+      float x[kC];
 #pragma unroll
-    for (int r = 0; r < kC; ++r) x[r] = G[r * kD + tid];
-    float run = 0.f;
+      for (int r = 0; r < kC; ++r) x[r] = G[r * kD + tid];
+      float run = 0.f;
 #pragma unroll
-    for (int r = 0; r < kC; ++r) {
-      run += fminf(fmaxf(x[r], a.g_min), 0.f) * kLog2e;
-      x[r] = run;
-    }
+      for (int r = 0; r < kC; ++r) {
+        run += fminf(fmaxf(x[r], a.g_min), 0.f) * kLog2e;
+        x[r] = run;
+      }
 #pragma unroll
-    for (int r = 0; r < kC; ++r) G[r * kD + tid] = x[r];
-  } else {
+      for (int r = 0; r < kC; ++r) G[r * kD + tid] = x[r];
+    } else {
 #pragma unroll 1
-    for (int i0 = 0; i0 < 32; i0 += 4) {  // rows rr = (warp - 4) + 4 i, i = i0 .. i0 + 3
-      float ss[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int rr = (warp - 4) + 4 * (i0 + u), r = rr & (kC - 1);
-        const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
-        const uint2 x = *reinterpret_cast<const uint2*>(src + lane * 8);
-        const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
-        const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
-        ss[u] = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
-      }
-      if (lane < 4) {  // lane u finishes row u of the group
-        const float sl = (lane == 0 ? ss[0] : lane == 1 ? ss[1] : lane == 2 ? ss[2] : ss[3]) +
-                         a.eps_l2;
-        const int rr = (warp - 4) + 4 * (i0 + lane), r = rr & (kC - 1);
-        const float inv = a.l2norm_qk ? (sl > 0.f ? rsqrtf(sl) : 0.f) : 1.f;
-        if (rr < kC) s_invq[r] = inv * a.q_scale;
-        else s_invk[r] = inv;
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- 3. Gram matrices: column tile b, 64-channel half kh at a time ----
-  //   A rows r >= 16b: [k^_r ; q^_r] * 2^(g_r - gend_b);  B rows j in tile b:
-  //   k^_j * 2^(gend_b - g_j); bf16 hi/lo; D[:, 16b..16b+15] += A B^T (3 products).
-  //   Pipelined: a round's operand items are computed into registers while the
-  //   previous round's MMAs still read the operand tiles, then stored.
-#pragma unroll 1
-  for (int round = 0; round < 8; ++round) {
-    const int b = round >> 1, kh = round & 1;
-    const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group), then 128 B items
-    // the decay at the end of tile b, for this thread's channel group (every
-    // item of this thread has the same group, 8 kh + tid % 8)
-    float ge[8];
-    ld8g(G + (16 * b + 15) * kD, 8 * kh + (tid & 7), ge);
-    uint4 iv0[3], iv1[3], iv2[3], iv3[3];
-    uint32_t io0[3], io1[3];
-    int kind[3];  // 0: none, 1: A item, 2: B item
-#pragma unroll
-    for (int s = 0; s < 3; ++s) {
-      const int it = tid + kPrepThreads * s;
-      kind[s] = it < nA ? 1 : (it < nA + 128 ? 2 : 0);
-      if (kind[s] == 1) {
-        const int r = 16 * b + (it >> 3), c8 = it & 7;
-        const int ch = 64 * kh + 8 * c8;
-        float g8[8], kf[8], qf[8];
-        ld8g(G + r * kD, 8 * kh + c8, g8);
-        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
-        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
-        const float ik = s_invk[r], iq = s_invq[r];
-        const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
-        uint32_t khi[4], klo[4], qhi[4], qlo[4];
+      for (int i0 = 0; i0 < 32; i0 += 4) {  // rows rr = (warp - 4) + 4 i, i = i0 .. i0 + 3
+        float ss[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float2 d = sub2(make_float2(g8[2 * u], g8[2 * u + 1]),
-                                make_float2(ge[2 * u], ge[2 * u + 1]));
-          const float2 e = make_float2(ex2f(d.x), ex2f(d.y));
-          split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]), mul2(e, ik2)), khi[u], klo[u]);
-          split2v(mul2(make_float2(qf[2 * u], qf[2 * u + 1]), mul2(e, iq2)), qhi[u], qlo[u]);
+          const int rr = (warp - 4) + 4 * (i0 + u), r = rr & (kC - 1);
+          const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
+          const uint2 x = *reinterpret_cast<const uint2*>(src + lane * 8);
+          const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+          const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+          ss[u] = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
         }
-        iv0[s] = make_uint4(khi[0], khi[1], khi[2], khi[3]);
-        iv1[s] = make_uint4(klo[0], klo[1], klo[2], klo[3]);
-        iv2[s] = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
-        iv3[s] = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
-        io0[s] = sw128_chunk(r, c8, 128);
-        io1[s] = sw128_chunk(64 + r, c8, 128);
-      } else if (kind[s] == 2) {
-        const int e = it - nA, jj = e >> 3, c8 = e & 7;
-        const int j = 16 * b + jj, ch = 64 * kh + 8 * c8;
-        float g8[8], kf[8];
-        ld8g(G + j * kD, 8 * kh + c8, g8);
-        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + ch * 2), kf);
-        const float ik = s_invk[j];
-        const float2 ik2 = make_float2(ik, ik);
-        uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 d = sub2(make_float2(ge[2 * u], ge[2 * u + 1]),
-                                make_float2(g8[2 * u], g8[2 * u + 1]));
-          split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]),
-                       mul2(make_float2(ex2f(d.x), ex2f(d.y)), ik2)), hi[u], lo[u]);
+        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
         }
-        iv0[s] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        iv1[s] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        io0[s] = sw128_chunk(jj, c8, 16);
+        if (lane < 4) {  // lane u finishes row u of the group
+          const float sl = (lane == 0 ? ss[0] : lane == 1 ? ss[1] : lane == 2 ? ss[2] : ss[3]) +
+                           a.eps_l2;
+          const int rr = (warp - 4) + 4 * (i0 + lane), r = rr & (kC - 1);
+          const float inv = a.l2norm_qk ? (sl > 0.f ? rsqrtf(sl) : 0.f) : 1.f;
+          if (rr < kC) s_invq[r] = inv * a.q_scale;
+          else s_invk[r] = inv;
+        }
       }
     }
-    bool waited = true;
-    if (round > 0) {  // the previous round's MMAs must be done reading the tiles
-      waited = mbar_wait(&bar_mma, mma_phase, t.spins);
-      mma_phase ^= 1;
-      fence_after_sync();
-    }
-#pragma unroll
-    for (int s = 0; s < 3; ++s) {
-      if (kind[s] == 1) {
-        *reinterpret_cast<uint4*>(sm + kPrepAhi + io0[s]) = iv0[s];
-        *reinterpret_cast<uint4*>(sm + kPrepAlo + io0[s]) = iv1[s];
-        *reinterpret_cast<uint4*>(sm + kPrepAhi + io1[s]) = iv2[s];
-        *reinterpret_cast<uint4*>(sm + kPrepAlo + io1[s]) = iv3[s];
-      } else if (kind[s] == 2) {
-        *reinterpret_cast<uint4*>(sm + kPrepBhi + io0[s]) = iv0[s];
-        *reinterpret_cast<uint4*>(sm + kPrepBlo + io0[s]) = iv1[s];
-      }
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(waited);
-    if (!ok) goto fail;
-    if (tid == 0) {
-      fence_after_sync();
-      // A_hi against [B_hi; B_lo] (one N = 32 product: the B_lo tile follows the
-      // B_hi tile as its rows 16..31) and A_lo against B_hi: A is read twice per
-      // K-step instead of three times
-      const uint32_t d = tmem + kGramCols * b;
-      const uint32_t ahi = smem_u32(sm + kPrepAhi), alo = smem_u32(sm + kPrepAlo);
-      const uint32_t bhi = smem_u32(sm + kPrepBhi);
-      const uint64_t dahi = desc_k_sw128(ahi, 0), dalo = desc_k_sw128(alo, 0);
-      const uint64_t dbhi = desc_k_sw128(bhi, 0);
-      // a K-step of 16 elements is 32 bytes: +2 in the descriptor's address field
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        const uint32_t acc = (kh | ks) ? 1u : 0u;
-        mma_ss(d, dahi + 2 * ks, dbhi + 2 * ks, kIdGram32, acc);
-        mma_ss(d + 32, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, acc);
-      }
-      mma_commit(&bar_mma);
-    }
-  }
-  ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
-  mma_phase ^= 1;
-  if (!ok) goto fail;
-  fence_after_sync();
+    __syncthreads();
 
-  {
-    // ---- 4. A (lanes 0..63) to shared memory, P (lanes 64..127) to the workspace ----
-    float* Amat = reinterpret_cast<float*>(sm + kPrepAmat);
-    {
-      const int quarter = warp & 3, chalf = warp >> 2;
-      const int r = quarter * 32 + lane;
-      uint32_t x[32];  // columns j = 32 chalf .. +31: tiles 2 chalf, 2 chalf + 1
+    // ---- 3. Gram matrices: column tile b, 64-channel half kh at a time ----
+    //   A rows r >= 16b: [k^_r ; q^_r] * 2^(g_r - gend_b);  B rows j in tile b:
+    //   k^_j * 2^(gend_b - g_j); bf16 hi/lo; D[:, 16b..16b+15] += A B^T (3 products).
+    //   Pipelined: a round's operand items are computed into registers while the
+    //   previous round's MMAs still read the operand tiles, then stored.
+#pragma unroll 1
+    for (int round = 0; round < 8; ++round) {
+      const int b = round >> 1, kh = round & 1;
+      const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group), then 128 B items
+      // the decay at the end of tile b, for this thread's channel group (every
+      // item of this thread has the same group, 8 kh + tid % 8)
+      float ge[8];
+      ld8g(G + (16 * b + 15) * kD, 8 * kh + (tid & 7), ge);
+      uint4 iv0[3], iv1[3], iv2[3], iv3[3];
+      uint32_t io0[3], io1[3];
+      int kind[3];  // 0: none, 1: A item, 2: B item
 #pragma unroll
-      for (int t2 = 0; t2 < 2; ++t2) {
-        uint32_t y[32], z[16];
-        const uint32_t col = kGramCols * (2 * chalf + t2);
-        tmem_ld32(taddr(tmem, quarter * 32, col), y);       // hi.hi | hi.lo
-        tmem_ld16(taddr(tmem, quarter * 32, col + 32), z);  // lo.hi
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          x[16 * t2 + j] = __float_as_uint(__uint_as_float(y[j]) + __uint_as_float(y[16 + j]) +
-                                           __uint_as_float(z[j]));
-      }
-      if (r < kC) {
-        const float br = s_beta[r];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int jj = 32 * chalf + j;
-          Amat[r * kAs + jj] = (jj < r) ? br * __uint_as_float(x[j]) : 0.f;
-        }
-      } else {
-        const int tr = r - kC;
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          uint32_t w[4];
+      for (int s = 0; s < 3; ++s) {
+        const int it = tid + kPrepThreads * s;
+        kind[s] = it < nA ? 1 : (it < nA + 128 ? 2 : 0);
+        if (kind[s] == 1) {
+          const int r = 16 * b + (it >> 3), c8 = it & 7;
+          const int ch = 64 * kh + 8 * c8;
+          float g8[8], kf[8], qf[8];
+          ld8g(G + r * kD, 8 * kh + c8, g8);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
+          const float ik = s_invk[r], iq = s_invq[r];
+          const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
+          uint32_t khi[4], klo[4], qhi[4], qlo[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int j0 = 8 * c8 + 2 * u, jj = 32 * chalf + j0;
-            w[u] = pack_half2(jj <= tr ? __uint_as_float(x[j0]) : 0.f,
-                              jj + 1 <= tr ? __uint_as_float(x[j0 + 1]) : 0.f);
+            const float2 d = sub2(make_float2(g8[2 * u], g8[2 * u + 1]),
+                                  make_float2(ge[2 * u], ge[2 * u + 1]));
+            const float2 e = make_float2(ex2f(d.x), ex2f(d.y));
+            split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]), mul2(e, ik2)), khi[u], klo[u]);
+            split2v(mul2(make_float2(qf[2 * u], qf[2 * u + 1]), mul2(e, iq2)), qhi[u], qlo[u]);
           }
-          *reinterpret_cast<uint4*>(ws + kWsP + sw128_chunk(tr, 4 * chalf + c8, 64)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-    }
-    fence_before_sync();
-    __syncthreads();
-
-    // ---- 5 / 6. Two warp groups in parallel (disjoint data, named barriers):
-    //      warps 4-7 run the row pass, warps 0-3 invert (I + A) ----
-    float* X = reinterpret_cast<float*>(sm + kPrepInv);
-    float* Y = reinterpret_cast<float*>(sm + kPrepY);
-    if (tid >= kPrepHalf) {
-      // ---- 5. row pass: -Q~ rows, K^ rows and G_C straight to the workspace, K~
-      //      (fp16) into the MN-major operand over the k rows; then the v rows, by
-      //      16-byte asynchronous copies (bf16, landing during the solve), into
-      //      the MN-major operand over the q rows.  Row item (row r, 8-channel
-      //      group c16) = rt + 128 m ----
-      const int rt = tid - kPrepHalf;
-      uint4 ktl[8];
-      const float* Gl = G + (kC - 1) * kD;
+          iv0[s] = make_uint4(khi[0], khi[1], khi[2], khi[3]);
+          iv1[s] = make_uint4(klo[0], klo[1], klo[2], klo[3]);
+          iv2[s] = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
+          iv3[s] = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
+          io0[s] = sw128_chunk(r, c8, 128);
+          io1[s] = sw128_chunk(64 + r, c8, 128);
+        } else if (kind[s] == 2) {
+          const int e = it - nA, jj = e >> 3, c8 = e & 7;
+          const int j = 16 * b + jj, ch = 64 * kh + 8 * c8;
+          float g8[8], kf[8];
+          ld8g(G + j * kD, 8 * kh + c8, g8);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + ch * 2), kf);
+          const float ik = s_invk[j];
+          const float2 ik2 = make_float2(ik, ik);
+          uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
-        float g8[8], gl8[8], kf[8], qf[8];
-        ld8g(G + r * kD, c16, g8);
-        ld8g(Gl, c16, gl8);
-        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
-        unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
-        const float ik = s_invk[r], iq = -s_invq[r];
-        const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
-        uint32_t wk[4], wq[4], wh[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 g2 = make_float2(g8[2 * u], g8[2 * u + 1]);
-          const float2 d = sub2(make_float2(gl8[2 * u], gl8[2 * u + 1]), g2);
-          const float2 e2 = make_float2(ex2f(g2.x), ex2f(g2.y));
-          const float2 f2 = make_float2(ex2f(d.x), ex2f(d.y));
-          const float2 k2 = mul2(make_float2(kf[2 * u], kf[2 * u + 1]), ik2);
-          const float2 q2 = mul2(make_float2(qf[2 * u], qf[2 * u + 1]), iq2);
-          const float2 kt2 = mul2(k2, e2), qt2 = mul2(q2, e2), kh2 = mul2(k2, f2);
-          wk[u] = pack_half2(kt2.x, kt2.y);
-          wq[u] = pack_half2(qt2.x, qt2.y);
-          wh[u] = pack_half2(kh2.x, kh2.y);
-        }
-        ktl[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-        *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(kC + r, c16, 128)) =
-            make_uint4(wq[0], wq[1], wq[2], wq[3]);
-        *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
-            make_uint4(wh[0], wh[1], wh[2], wh[3]);
-      }
-      reinterpret_cast<float*>(ws + kWsGam)[rt] = ex2f(Gl[gpos(rt)]);
-      named_sync(kBarRow, kPrepHalf);  // every read of the q, k rows is done: they take K~, V
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15;
-        *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = ktl[m];
-        const int rr = r < len ? r : 0;
-        cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
-                   v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
-      }
-      cp_async_commit();
-    } else {
-      // ---- 6. X = (I + A)^-1 by 16 x 16 blocks ----
-      if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
-        const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update
-        float x[16];                                          // rows below: 15-FMA chain)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < 15; ++m) {
-#pragma unroll
-          for (int r = m + 1; r < 16; ++r) x[r] -= Amat[(o + r) * kAs + o + m] * x[m];
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
-      } else {  // the blocks above the diagonal are zero
-        for (int e = tid - 64; e < 6 * 256; e += kPrepHalf - 64) {
-          const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-          const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-          const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-          X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
-        }
-      }
-      named_sync(kBarSolve, kPrepHalf);
-      // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj.
-      // The sum is split by 16-token tile p of m: unrolled 16-term products (4
-      // adjacent columns of one row, float4 loads), partial sums in Y.
-#pragma unroll
-      for (int dd = 1; dd < 4; ++dd) {
-        const int nblk = 4 - dd;
-        for (int u = tid; u < nblk * dd * 64; u += kPrepHalf) {
-          const int p = u / (nblk * 64), rem = u - p * (nblk * 64);
-          const int bj = rem >> 6, bi = bj + dd, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
-          const int m0 = 16 * (bj + p);
-          const float* arow = Amat + (16 * bi + r) * kAs + m0;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int mm = 0; mm < 16; ++mm) {
-            const float am = arow[mm];
-            const float4 x4 =
-                *reinterpret_cast<const float4*>(X + (m0 + mm) * kXs + 16 * bj + c4);
-            acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+          for (int u = 0; u < 4; ++u) {
+            const float2 d = sub2(make_float2(ge[2 * u], ge[2 * u + 1]),
+                                  make_float2(g8[2 * u], g8[2 * u + 1]));
+            split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]),
+                         mul2(make_float2(ex2f(d.x), ex2f(d.y)), ik2)), hi[u], lo[u]);
           }
-          *reinterpret_cast<float4*>(Y + ((p * nblk + bj) << 8) + r * 16 + c4) = acc;
+          iv0[s] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          iv1[s] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          io0[s] = sw128_chunk(jj, c8, 16);
         }
-        named_sync(kBarSolve, kPrepHalf);
-        for (int u = tid; u < nblk * 64; u += kPrepHalf) {
-          const int bj = u >> 6, bi = bj + dd, r = (u >> 2) & 15, c4 = (u & 3) * 4;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
+      }
+      bool waited = true;
+      if (round > 0) {  // the previous round's MMAs must be done reading the tiles
+        waited = mbar_wait(&bar_mma, mma_phase, t.spins);
+        mma_phase ^= 1;
+        fence_after_sync();
+      }
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float xm = xrow[m];
-            float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
-#pragma unroll
-            for (int pp = 1; pp < dd; ++pp) {
-              const float4 z4 =
-                  *reinterpret_cast<const float4*>(Y + ((pp * nblk + bj) << 8) + m * 16 + c4);
-              y4.x += z4.x; y4.y += z4.y; y4.z += z4.z; y4.w += z4.w;
-            }
-            acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
-          }
-          *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
-              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+      for (int s = 0; s < 3; ++s) {
+        if (kind[s] == 1) {
+          *reinterpret_cast<uint4*>(sm + kPrepAhi + io0[s]) = iv0[s];
+          *reinterpret_cast<uint4*>(sm + kPrepAlo + io0[s]) = iv1[s];
+          *reinterpret_cast<uint4*>(sm + kPrepAhi + io1[s]) = iv2[s];
+          *reinterpret_cast<uint4*>(sm + kPrepAlo + io1[s]) = iv3[s];
+        } else if (kind[s] == 2) {
+          *reinterpret_cast<uint4*>(sm + kPrepBhi + io0[s]) = iv0[s];
+          *reinterpret_cast<uint4*>(sm + kPrepBlo + io0[s]) = iv1[s];
         }
-        named_sync(kBarSolve, kPrepHalf);
       }
-    }
-    __syncthreads();  // X, the workspace rows, K~ and the v copies are all issued
-
-    // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
-    //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
-    //      decay rows for the U~ product (V stays exact in bf16) ----
-    for (int e = tid; e < kC * 8; e += kPrepThreads) {
-      const int tr = e >> 3, c8 = e & 7;
-      uint32_t w[4], th[4], tl[4];
+      fence_proxy_async();
+      fence_before_sync();
+      ok = __syncthreads_and(waited);
+      if (!ok) goto fail;
+      if (tid == 0) {
+        fence_after_sync();
+        // A_hi against [B_hi; B_lo] (one N = 32 product: the B_lo tile follows the
+        // B_hi tile as its rows 16..31) and A_lo against B_hi: A is read twice per
+        // K-step instead of three times
+        const uint32_t d = tmem + kGramCols * b;
+        const uint32_t ahi = smem_u32(sm + kPrepAhi), alo = smem_u32(sm + kPrepAlo);
+        const uint32_t bhi = smem_u32(sm + kPrepBhi);
+        const uint64_t dahi = desc_k_sw128(ahi, 0), dalo = desc_k_sw128(alo, 0);
+        const uint64_t dbhi = desc_k_sw128(bhi, 0);
+        // a K-step of 16 elements is 32 bytes: +2 in the descriptor's address field
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j0 = 8 * c8 + 2 * u;
-        const float2 x2 = *reinterpret_cast<const float2*>(X + tr * kXs + j0);
-        const float2 t2 = make_float2(x2.x * s_beta[j0], x2.y * s_beta[j0 + 1]);
-        w[u] = pack_half2(t2.x, t2.y);
-        split2v(t2, th[u], tl[u]);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t acc = (kh | ks) ? 1u : 0u;
+          mma_ss(d, dahi + 2 * ks, dbhi + 2 * ks, kIdGram32, acc);
+          mma_ss(d + 32, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, acc);
+        }
+        mma_commit(&bar_mma);
       }
-      const uint4 wt = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(tr, c8, 128)) = wt;
-      *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(kC + tr, c8, 128)) = wt;
-      *reinterpret_cast<uint4*>(sm + kPrepThi + sw128_chunk(tr, c8, kC)) =
-          make_uint4(th[0], th[1], th[2], th[3]);
-      *reinterpret_cast<uint4*>(sm + kPrepTlo + sw128_chunk(tr, c8, kC)) =
-          make_uint4(tl[0], tl[1], tl[2], tl[3]);
-    }
-    cp_async_wait_all();  // this thread's v rows have landed
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-
-    // ---- 8. U~^T = V^T (T_hi + T_lo)^T (A = V MN-major bf16) and W = [T; T] K~
-    //      (B = K~ MN-major fp16) on the tensor cores, then both straight to the
-    //      workspace ----
-    if (tid == 0) {
-      fence_after_sync();
-      const uint32_t sT = smem_u32(sm + kPrepTT), sV = smem_u32(sm + kPrepV);
-      const uint32_t sKt = smem_u32(sm + kPrepKt);
-      const uint32_t sTh = smem_u32(sm + kPrepThi), sTl = smem_u32(sm + kPrepTlo);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTh, 32 * ks),
-               kIdUt, ks > 0);
-        mma_ss(tmem + kTdW, desc_k_sw128(sT, 32 * ks), desc_mn_sw128(sKt, ks, kC * 128),
-               kIdW, ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTl, 32 * ks),
-               kIdUt, 1u);
-      mma_commit(&bar_mma);
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
     mma_phase ^= 1;
     if (!ok) goto fail;
     fence_after_sync();
+
     {
-      // warp (quarter, chalf): U~^T rows ch = its TMEM lanes, columns t = 32 chalf ..;
-      // W rows t = its lanes mod 64 (both copies), 32-column slab 2 chalf + quarter / 2
-      const int quarter = warp & 3, chalf = warp >> 2;
-      const int lrow = quarter * 32 + lane, slab = 2 * chalf + (quarter >> 1);
-      uint32_t x[32], y[32];
-      tmem_ld32(taddr(tmem, quarter * 32, kTdU + 32 * chalf), x);
-      tmem_ld32(taddr(tmem, quarter * 32, kTdW + 32 * slab), y);
-      tmem_wait_ld();
+      // ---- 4. A (lanes 0..63) to shared memory, P (lanes 64..127) to the workspace ----
+      float* Amat = reinterpret_cast<float*>(sm + kPrepAmat);
+      {
+        const int quarter = warp & 3, chalf = warp >> 2;
+        const int r = quarter * 32 + lane;
+        uint32_t x[32];  // columns j = 32 chalf .. +31: tiles 2 chalf, 2 chalf + 1
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint32_t w[4];
+        for (int t2 = 0; t2 < 2; ++t2) {
+          uint32_t y[32], z[16];
+          const uint32_t col = kGramCols * (2 * chalf + t2);
+          tmem_ld32(taddr(tmem, quarter * 32, col), y);       // hi.hi | hi.lo
+          tmem_ld16(taddr(tmem, quarter * 32, col + 32), z);  // lo.hi
+          tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          w[u] = pack_half2(__uint_as_float(x[8 * c8 + 2 * u]), __uint_as_float(x[8 * c8 + 2 * u + 1]));
-        *reinterpret_cast<uint4*>(ws + kWsUt + sw128_chunk(lrow, 4 * chalf + c8, 128)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+          for (int j = 0; j < 16; ++j)
+            x[16 * t2 + j] = __float_as_uint(__uint_as_float(y[j]) + __uint_as_float(y[16 + j]) +
+                                             __uint_as_float(z[j]));
+        }
+        if (r < kC) {
+          const float br = s_beta[r];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int jj = 32 * chalf + j;
+            Amat[r * kAs + jj] = (jj < r) ? br * __uint_as_float(x[j]) : 0.f;
+          }
+        } else {
+          const int tr = r - kC;
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j0 = 8 * c8 + 2 * u, jj = 32 * chalf + j0;
+              w[u] = pack_half2(jj <= tr ? __uint_as_float(x[j0]) : 0.f,
+                                jj + 1 <= tr ? __uint_as_float(x[j0 + 1]) : 0.f);
+            }
+            *reinterpret_cast<uint4*>(ws + kWsP + sw128_chunk(tr, 4 * chalf + c8, 64)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
-      const int tw = lrow & (kC - 1);
+      fence_before_sync();
+      __syncthreads();
+
+      // ---- 5 / 6. Two warp groups in parallel (disjoint data, named barriers):
+      //      warps 4-7 run the row pass, warps 0-3 invert (I + A) ----
+      float* X = reinterpret_cast<float*>(sm + kPrepInv);
+      float* Y = reinterpret_cast<float*>(sm + kPrepY);
+      if (tid >= kPrepHalf) {
+        // ---- 5. row pass: -Q~ rows, K^ rows and G_C straight to the workspace, K~
+        //      (fp16) into the MN-major operand over the k rows; then the v rows, by
+        //      16-byte asynchronous copies (bf16, landing during the solve), into
+        //      the MN-major operand over the q rows.  Row item (row r, 8-channel
+        //      group c16) = rt + 128 m ----
+        const int rt = tid - kPrepHalf;
+        // K~ of the 8 items waits in TMEM (columns kTdScratch.., this thread's lane)
+        // until every read of the k rows is done
+        const uint32_t scratch = taddr(tmem, (warp & 3) * 32, kTdScratch);
+        const float* Gl = G + (kC - 1) * kD;
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint32_t w[4];
+        for (int m = 0; m < 8; ++m) {
+          const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
+          float g8[8], gl8[8], kf[8], qf[8];
+          ld8g(G + r * kD, c16, g8);
+          ld8g(Gl, c16, gl8);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
+          const float ik = s_invk[r], iq = -s_invq[r];
+          const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
+          uint32_t wk[4], wq[4], wh[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          w[u] = pack_half2(__uint_as_float(y[8 * c8 + 2 * u]), __uint_as_float(y[8 * c8 + 2 * u + 1]));
-        *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(tw, 4 * slab + c8, 128)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+          for (int u = 0; u < 4; ++u) {
+            const float2 g2 = make_float2(g8[2 * u], g8[2 * u + 1]);
+            const float2 d = sub2(make_float2(gl8[2 * u], gl8[2 * u + 1]), g2);
+            const float2 e2 = make_float2(ex2f(g2.x), ex2f(g2.y));
+            const float2 f2 = make_float2(ex2f(d.x), ex2f(d.y));
+            const float2 k2 = mul2(make_float2(kf[2 * u], kf[2 * u + 1]), ik2);
+            const float2 q2 = mul2(make_float2(qf[2 * u], qf[2 * u + 1]), iq2);
+            const float2 kt2 = mul2(k2, e2), qt2 = mul2(q2, e2), kh2 = mul2(k2, f2);
+            wk[u] = pack_half2(kt2.x, kt2.y);
+            wq[u] = pack_half2(qt2.x, qt2.y);
+            wh[u] = pack_half2(kh2.x, kh2.y);
+          }
+          tmem_st4(scratch + 4 * m, wk[0], wk[1], wk[2], wk[3]);
+          *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(kC + r, c16, 128)) =
+              make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
+              make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        }
+        reinterpret_cast<float*>(ws + kWsGam)[rt] = ex2f(Gl[gpos(rt)]);
+        tmem_wait_st();
+        named_sync(kBarRow, kPrepHalf);  // every read of the q, k rows is done: they take K~, V
+        uint32_t ktl[32];
+        tmem_ld32(scratch, ktl);
+        tmem_wait_ld();
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15;
+          *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) =
+              make_uint4(ktl[4 * m], ktl[4 * m + 1], ktl[4 * m + 2], ktl[4 * m + 3]);
+          const int rr = r < len ? r : 0;
+          cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
+                     v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
+        }
+        cp_async_commit();
+      } else {
+        // ---- 6. X = (I + A)^-1 by 16 x 16 blocks ----
+        if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
+          const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update
+          float x[16];                                          // rows below: 15-FMA chain)
+#pragma unroll
+          for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+          for (int m = 0; m < 15; ++m) {
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r) x[r] -= Amat[(o + r) * kAs + o + m] * x[m];
+          }
+#pragma unroll
+          for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
+        } else {  // the blocks above the diagonal are zero
+          for (int e = tid - 64; e < 6 * 256; e += kPrepHalf - 64) {
+            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+            X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
+          }
+        }
+        named_sync(kBarSolve, kPrepHalf);
+        // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj.
+        // The sum is split by 16-token tile p of m: unrolled 16-term products (4
+        // adjacent columns of one row, float4 loads), partial sums in Y.
+#pragma unroll
+        for (int dd = 1; dd < 4; ++dd) {
+          const int nblk = 4 - dd;
+          for (int u = tid; u < nblk * dd * 64; u += kPrepHalf) {
+            const int p = u / (nblk * 64), rem = u - p * (nblk * 64);
+            const int bj = rem >> 6, bi = bj + dd, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
+            const int m0 = 16 * (bj + p);
+            const float* arow = Amat + (16 * bi + r) * kAs + m0;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int mm = 0; mm < 16; ++mm) {
+              const float am = arow[mm];
+              const float4 x4 =
+                  *reinterpret_cast<const float4*>(X + (m0 + mm) * kXs + 16 * bj + c4);
+              acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+            }
+            *reinterpret_cast<float4*>(Y + ((p * nblk + bj) << 8) + r * 16 + c4) = acc;
+          }
+          named_sync(kBarSolve, kPrepHalf);
+          for (int u = tid; u < nblk * 64; u += kPrepHalf) {
+            const int bj = u >> 6, bi = bj + dd, r = (u >> 2) & 15, c4 = (u & 3) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const float xm = xrow[m];
+              float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
+#pragma unroll
+              for (int pp = 1; pp < dd; ++pp) {
+                const float4 z4 =
+                    *reinterpret_cast<const float4*>(Y + ((pp * nblk + bj) << 8) + m * 16 + c4);
+                y4.x += z4.x; y4.y += z4.y; y4.z += z4.z; y4.w += z4.w;
+              }
+              acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
+            }
+            *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+          }
+          named_sync(kBarSolve, kPrepHalf);
+        }
       }
+      __syncthreads();  // X, the workspace rows, K~ and the v copies are all issued
+
+      // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
+      //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
+      //      decay rows for the U~ product (V stays exact in bf16) ----
+      for (int e = tid; e < kC * 8; e += kPrepThreads) {
+        const int tr = e >> 3, c8 = e & 7;
+        uint32_t w[4], th[4], tl[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j0 = 8 * c8 + 2 * u;
+          const float2 x2 = *reinterpret_cast<const float2*>(X + tr * kXs + j0);
+          const float2 t2 = make_float2(x2.x * s_beta[j0], x2.y * s_beta[j0 + 1]);
+          w[u] = pack_half2(t2.x, t2.y);
+          split2v(t2, th[u], tl[u]);
+        }
+        const uint4 wt = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(tr, c8, 128)) = wt;
+        *reinterpret_cast<uint4*>(sm + kPrepTT + sw128_chunk(kC + tr, c8, 128)) = wt;
+        *reinterpret_cast<uint4*>(sm + kPrepThi + sw128_chunk(tr, c8, kC)) =
+            make_uint4(th[0], th[1], th[2], th[3]);
+        *reinterpret_cast<uint4*>(sm + kPrepTlo + sw128_chunk(tr, c8, kC)) =
+            make_uint4(tl[0], tl[1], tl[2], tl[3]);
+      }
+      cp_async_wait_all();  // this thread's v rows have landed
+      fence_proxy_async();
+      fence_before_sync();
+      __syncthreads();
+
+      // ---- 8. U~^T = V^T (T_hi + T_lo)^T (A = V MN-major bf16) and W = [T; T] K~
+      //      (B = K~ MN-major fp16) on the tensor cores, then both straight to the
+      //      workspace ----
+      if (tid == 0) {
+        fence_after_sync();
+        const uint32_t sT = smem_u32(sm + kPrepTT), sV = smem_u32(sm + kPrepV);
+        const uint32_t sKt = smem_u32(sm + kPrepKt);
+        const uint32_t sTh = smem_u32(sm + kPrepThi), sTl = smem_u32(sm + kPrepTlo);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTh, 32 * ks),
+                 kIdUt, ks > 0);
+          mma_ss(tmem + kTdW, desc_k_sw128(sT, 32 * ks), desc_mn_sw128(sKt, ks, kC * 128),
+                 kIdW, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTl, 32 * ks),
+                 kIdUt, 1u);
+        mma_commit(&bar_mma);
+      }
+      ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
+      mma_phase ^= 1;
+      if (!ok) goto fail;
+      fence_after_sync();
+      // the products are done with every buffer: the next item's inputs stream in
+      // while this one's results leave TMEM
+      const int w_next = item + (int)gridDim.x;
+      int gid_n = 0, h_n = 0, tok0_n = 0, len_n = 0;
+      if (w_next < items) {
+        decode(w_next, gid_n, h_n, tok0_n, len_n);
+        issue_inputs(h_n, tok0_n, len_n);
+      }
+      {
+        // warp (quarter, chalf): U~^T rows ch = its TMEM lanes, columns t = 32 chalf ..;
+        // W rows t = its lanes mod 64 (both copies), 32-column slab 2 chalf + quarter / 2
+        const int quarter = warp & 3, chalf = warp >> 2;
+        const int lrow = quarter * 32 + lane, slab = 2 * chalf + (quarter >> 1);
+        uint32_t x[32], y[32];
+        tmem_ld32(taddr(tmem, quarter * 32, kTdU + 32 * chalf), x);
+        tmem_ld32(taddr(tmem, quarter * 32, kTdW + 32 * slab), y);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w[u] = pack_half2(__uint_as_float(x[8 * c8 + 2 * u]), __uint_as_float(x[8 * c8 + 2 * u + 1]));
+          *reinterpret_cast<uint4*>(ws + kWsUt + sw128_chunk(lrow, 4 * chalf + c8, 128)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        const int tw = lrow & (kC - 1);
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w[u] = pack_half2(__uint_as_float(y[8 * c8 + 2 * u]), __uint_as_float(y[8 * c8 + 2 * u + 1]));
+          *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(tw, 4 * slab + c8, 128)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      if (w_next >= items) break;
+      item = w_next;
+      gid = gid_n;
+      h = h_n;
+      tok0 = tok0_n;
+      len = len_n;
     }
   }
   goto done;
@@ -1158,9 +1191,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
   cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(opt->phase_events);
   cudaError_t e;
   static bool attr_done[64] = {false};
+  static int sm_count[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPrepSmem);
     if (e != cudaSuccess) return e;
@@ -1174,8 +1210,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return e;
   if (t.total_chunks_max > 0 && !t.debug_timeout) {
-    dim3 grid((unsigned)t.total_chunks_max, (unsigned)a.H);
-    prep_kernel<<<grid, kPrepThreads, kPrepSmem, s>>>(t);
+    // persistent: two CTAs per SM walk the (chunk, head) items
+    const long long items_max = (long long)t.total_chunks_max * a.H;
+    const long long resident = 2LL * (dev >= 0 && dev < 64 ? sm_count[dev] : 148);
+    prep_kernel<<<(unsigned)(items_max < resident ? items_max : resident), kPrepThreads,
+                  kPrepSmem, s>>>(t);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return e;
