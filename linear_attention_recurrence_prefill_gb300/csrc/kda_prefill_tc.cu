@@ -638,48 +638,66 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           }
         }
         named_sync(kBarSolve, kPrepHalf);
-        // off-diagonal blocks by distance dd = i - j: X_ij = -X_ii sum_{m=j}^{i-1} A_im X_mj.
-        // The sum is split by 16-token tile p of m: unrolled 16-term products (4
-        // adjacent columns of one row, float4 loads), partial sums in Y.
+        // 2 x 2 block inverse at 32 x 32: the lower 16 x 16 block of each diagonal
+        // 32-block, X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (B1, B2),
+        // then the lower 32-block, X_10 = -X_11 A_10 X_00 in 32-blocks (C1, C2).
+        // Each unit is 4 adjacent columns of one row (float4 loads), unrolled.
+        {  // B1: Y_p = A_{2p+1,2p} X_{2p,2p}; unit (p, r, c4)
+          const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+          const int i1 = 16 * (2 * p + 1), i0 = 32 * p;
+          const float* arow = Amat + (i1 + r) * kAs + i0;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int dd = 1; dd < 4; ++dd) {
-          const int nblk = 4 - dd;
-          for (int u = tid; u < nblk * dd * 64; u += kPrepHalf) {
-            const int p = u / (nblk * 64), rem = u - p * (nblk * 64);
-            const int bj = rem >> 6, bi = bj + dd, r = (rem >> 2) & 15, c4 = (rem & 3) * 4;
-            const int m0 = 16 * (bj + p);
-            const float* arow = Amat + (16 * bi + r) * kAs + m0;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int mm = 0; mm < 16; ++mm) {
-              const float am = arow[mm];
-              const float4 x4 =
-                  *reinterpret_cast<const float4*>(X + (m0 + mm) * kXs + 16 * bj + c4);
-              acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
-            }
-            *reinterpret_cast<float4*>(Y + ((p * nblk + bj) << 8) + r * 16 + c4) = acc;
+          for (int m = 0; m < 16; ++m) {
+            const float am = arow[m];
+            const float4 x4 = *reinterpret_cast<const float4*>(X + (i0 + m) * kXs + i0 + c4);
+            acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
           }
-          named_sync(kBarSolve, kPrepHalf);
-          for (int u = tid; u < nblk * 64; u += kPrepHalf) {
-            const int bj = u >> 6, bi = bj + dd, r = (u >> 2) & 15, c4 = (u & 3) * 4;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float* xrow = X + (16 * bi + r) * kXs + 16 * bi;
+          *reinterpret_cast<float4*>(Y + (p << 8) + r * 16 + c4) = acc;
+        }
+        named_sync(kBarSolve, kPrepHalf);
+        {  // B2: X_{2p+1,2p} = -X_{2p+1,2p+1} Y_p
+          const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+          const int i1 = 16 * (2 * p + 1), i0 = 32 * p;
+          const float* xrow = X + (i1 + r) * kXs + i1;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-              const float xm = xrow[m];
-              float4 y4 = *reinterpret_cast<const float4*>(Y + (bj << 8) + m * 16 + c4);
-#pragma unroll
-              for (int pp = 1; pp < dd; ++pp) {
-                const float4 z4 =
-                    *reinterpret_cast<const float4*>(Y + ((pp * nblk + bj) << 8) + m * 16 + c4);
-                y4.x += z4.x; y4.y += z4.y; y4.z += z4.z; y4.w += z4.w;
-              }
-              acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
-            }
-            *reinterpret_cast<float4*>(X + (16 * bi + r) * kXs + 16 * bj + c4) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+          for (int m = 0; m < 16; ++m) {
+            const float xm = xrow[m];
+            const float4 y4 = *reinterpret_cast<const float4*>(Y + (p << 8) + m * 16 + c4);
+            acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
           }
-          named_sync(kBarSolve, kPrepHalf);
+          *reinterpret_cast<float4*>(X + (i1 + r) * kXs + i0 + c4) =
+              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        named_sync(kBarSolve, kPrepHalf);
+#pragma unroll 1
+        for (int u = tid; u < 256; u += kPrepHalf) {  // C1: Z = A_10 X_00 (32-blocks)
+          const int r = u >> 3, c4 = (u & 7) * 4;
+          const float* arow = Amat + (32 + r) * kAs;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+          for (int m = 0; m < 32; ++m) {
+            const float am = arow[m];
+            const float4 x4 = *reinterpret_cast<const float4*>(X + m * kXs + c4);
+            acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+          }
+          *reinterpret_cast<float4*>(Y + r * 32 + c4) = acc;
+        }
+        named_sync(kBarSolve, kPrepHalf);
+#pragma unroll 1
+        for (int u = tid; u < 256; u += kPrepHalf) {  // C2: X_10 = -X_11 Z
+          const int r = u >> 3, c4 = (u & 7) * 4;
+          const float* xrow = X + (32 + r) * kXs + 32;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+          for (int m = 0; m < 32; ++m) {
+            const float xm = xrow[m];
+            const float4 z4 = *reinterpret_cast<const float4*>(Y + m * 32 + c4);
+            acc.x += xm * z4.x; acc.y += xm * z4.y; acc.z += xm * z4.z; acc.w += xm * z4.w;
+          }
+          *reinterpret_cast<float4*>(X + (32 + r) * kXs + c4) =
+              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
       }
       __syncthreads();  // X, the workspace rows, K~ and the v copies are all issued
