@@ -639,9 +639,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         }
         named_sync(kBarSolve, kPrepHalf);
         // 2 x 2 block inverse at 32 x 32: the lower 16 x 16 block of each diagonal
-        // 32-block, X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (B1, B2),
-        // then the lower 32-block, X_10 = -X_11 A_10 X_00 in 32-blocks (C1, C2).
-        // Each unit is 4 adjacent columns of one row (float4 loads), unrolled.
+        // 32-block, X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (B1, B2);
+        // the lower 32-block follows below with all threads (C1, C2).  Each unit
+        // is 4 adjacent columns of one row (float4 loads), unrolled.
         {  // B1: Y_p = A_{2p+1,2p} X_{2p,2p}; unit (p, r, c4)
           const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
           const int i1 = 16 * (2 * p + 1), i0 = 32 * p;
@@ -670,35 +670,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           *reinterpret_cast<float4*>(X + (i1 + r) * kXs + i0 + c4) =
               make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
-        named_sync(kBarSolve, kPrepHalf);
-#pragma unroll 1
-        for (int u = tid; u < 256; u += kPrepHalf) {  // C1: Z = A_10 X_00 (32-blocks)
-          const int r = u >> 3, c4 = (u & 7) * 4;
-          const float* arow = Amat + (32 + r) * kAs;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncthreads();  // the diagonal 32-blocks of X are complete; the row pass is issued
+      // the lower 32-block, X_10 = -X_11 A_10 X_00, by all threads: unit = (row r,
+      // 4 columns c4) of the 32 x 32 block
+      {  // C1: Z = A_10 X_00
+        const int r = tid >> 3, c4 = (tid & 7) * 4;
+        const float* arow = Amat + (32 + r) * kAs;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-          for (int m = 0; m < 32; ++m) {
-            const float am = arow[m];
-            const float4 x4 = *reinterpret_cast<const float4*>(X + m * kXs + c4);
-            acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
-          }
-          *reinterpret_cast<float4*>(Y + r * 32 + c4) = acc;
+        for (int m = 0; m < 32; ++m) {
+          const float am = arow[m];
+          const float4 x4 = *reinterpret_cast<const float4*>(X + m * kXs + c4);
+          acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
         }
-        named_sync(kBarSolve, kPrepHalf);
-#pragma unroll 1
-        for (int u = tid; u < 256; u += kPrepHalf) {  // C2: X_10 = -X_11 Z
-          const int r = u >> 3, c4 = (u & 7) * 4;
-          const float* xrow = X + (32 + r) * kXs + 32;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(Y + r * 32 + c4) = acc;
+      }
+      __syncthreads();
+      {  // C2: X_10 = -X_11 Z
+        const int r = tid >> 3, c4 = (tid & 7) * 4;
+        const float* xrow = X + (32 + r) * kXs + 32;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
-          for (int m = 0; m < 32; ++m) {
-            const float xm = xrow[m];
-            const float4 z4 = *reinterpret_cast<const float4*>(Y + m * 32 + c4);
-            acc.x += xm * z4.x; acc.y += xm * z4.y; acc.z += xm * z4.z; acc.w += xm * z4.w;
-          }
-          *reinterpret_cast<float4*>(X + (32 + r) * kXs + c4) =
-              make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        for (int m = 0; m < 32; ++m) {
+          const float xm = xrow[m];
+          const float4 z4 = *reinterpret_cast<const float4*>(Y + m * 32 + c4);
+          acc.x += xm * z4.x; acc.y += xm * z4.y; acc.z += xm * z4.z; acc.w += xm * z4.w;
         }
+        *reinterpret_cast<float4*>(X + (32 + r) * kXs + c4) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
       __syncthreads();  // X, the workspace rows, K~ and the v copies are all issued
 
