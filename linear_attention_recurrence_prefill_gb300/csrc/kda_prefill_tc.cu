@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     __syncthreads();
 
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
-    //      registers); L2 norms of the q, k rows (warps 4-7, four rows at a time) ----
+    //      registers); L2 norms of the q, k rows (warps 4-7, one row per thread) ----
     if (tid < kD) {  // thread tid scans word tid of the rows (whichever channel it holds)
       float x[kC];
 #pragma unroll
@@ -368,32 +368,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
       for (int r = 0; r < kC; ++r) G[r * kD + tid] = x[r];
     } else {
-#pragma unroll 1
-      for (int i0 = 0; i0 < 32; i0 += 4) {  // rows rr = (warp - 4) + 4 i, i = i0 .. i0 + 3
-        float ss[4];
+      // one row per thread (q rows 0..63, then k rows): its sixteen 16-byte chunks
+      // in an order rotated by the row, so that a warp's loads hit every bank
+      const int rr = tid - kD, r = rr & (kC - 1);
+      const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src + (((i + rr) & 15) << 4));
+        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int rr = (warp - 4) + 4 * (i0 + u), r = rr & (kC - 1);
-          const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
-          const uint2 x = *reinterpret_cast<const uint2*>(src + lane * 8);
-          const float2 x0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
-          const float2 x1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
-          ss[u] = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
-        }
-        if (lane < 4) {  // lane u finishes row u of the group
-          const float sl = (lane == 0 ? ss[0] : lane == 1 ? ss[1] : lane == 2 ? ss[2] : ss[3]) +
-                           a.eps_l2;
-          const int rr = (warp - 4) + 4 * (i0 + lane), r = rr & (kC - 1);
-          const float inv = a.l2norm_qk ? (sl > 0.f ? rsqrtf(sl) : 0.f) : 1.f;
-          if (rr < kC) s_invq[r] = inv * a.q_scale;
-          else s_invk[r] = inv;
+          const float lo = __uint_as_float(wv[u] << 16), hi = __uint_as_float(wv[u] & 0xFFFF0000u);
+          s4[u] = fmaf(lo, lo, s4[u]);
+          s4[u] = fmaf(hi, hi, s4[u]);
         }
       }
+      const float sl = (s4[0] + s4[1]) + (s4[2] + s4[3]) + a.eps_l2;
+      const float inv = a.l2norm_qk ? (sl > 0.f ? rsqrtf(sl) : 0.f) : 1.f;
+      if (rr < kC) s_invq[r] = inv * a.q_scale;
+      else s_invk[r] = inv;
     }
     __syncthreads();
 
