@@ -2,9 +2,8 @@
 //
 // One CTA walks one (sequence, head) pair chunk by chunk (16 tokens), keeping
 // the d x d state in shared memory.  Inside a chunk the work is parallel; the
-// chunks follow one another ("KDA trains chunkwise, in parallel inside a chunk
-// and recurrently across chunks": "Kimi K3's hybrid block, from first
-// principles", section "From linear attention to the delta rule").
+// chunks follow one another through the state ("Kimi K3's hybrid block, from
+// first principles", section "From linear attention to the delta rule").
 //
 // Chunk algebra (exactly the token recurrence, regrouped).  With state S at the
 // chunk start, g_t the inclusive running sum of the clamped log-decays from the

@@ -1,12 +1,13 @@
 // kda_prefill_tc.cu -- chunked KDA prefill on the tcgen05 tensor cores (sm_103a).
 //
 // The layer is processed in chunks of C = 64 tokens, each split into four
-// 16-token tiles ("KDA trains chunkwise, in parallel inside a chunk and
-// recurrently across chunks ... Over a 16-token tile the cumulative log-decay
-// stays within (-80, 0), so the rescaling factors fit in BF16's range and every
-// tile, including the diagonal ones, runs as dense tensor-core matrix
-// multiplies": "Kimi K3's hybrid block, from first principles", section "From
-// linear attention to the delta rule").  Three kernels per call:
+// 16-token tiles.  Inside a chunk all tokens are handled at once and the chunks
+// follow one another through the state; with log alpha >= -5 the running
+// log-decay changes by less than 80 over a tile, so every decay factor taken
+// relative to a tile boundary lies within e^-80 .. e^80 (inside the bf16 / fp32
+// exponent range) and every tile, the diagonal ones included, is a dense
+// tensor-core product ("Kimi K3's hybrid block, from first principles", section
+// "From linear attention to the delta rule").  Three kernels per call:
 //
 //   1. chunk_base_kernel   prefix sum of chunks per sequence (varlen support).
 //   2. prep_kernel         one CTA per (chunk, head), all chunks in parallel:
@@ -288,9 +289,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   fence_after_sync();
   const uint32_t tmem = tmem_base;
 
+  // sequences of one length L (no cu_seqlens) have ceil(L / C) chunks each: the
+  // item's tokens follow by arithmetic, without a dependent load
+  const int L_eq = a.cu_seqlens ? 0 : a.T_total / a.N;
+  const int cps_eq = (L_eq + kC - 1) / kC;
   auto decode = [&](int wi, int& gid_, int& h_, int& tok0_, int& len_) {
     h_ = wi / total;
     gid_ = wi - h_ * total;
+    if (!a.cu_seqlens) {
+      const int n_ = gid_ / cps_eq;
+      tok0_ = n_ * L_eq + (gid_ - n_ * cps_eq) * kC;
+      len_ = min(kC, (n_ + 1) * L_eq - tok0_);
+      return;
+    }
     const int n_ = find_seq(t.chunk_base, a.N, gid_);
     int s0_, s1_;
     seq_range(a.cu_seqlens, a.N, a.T_total, n_, s0_, s1_);
@@ -333,14 +344,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         *reinterpret_cast<float4*>(sm + kPrepG + r * 512 + wd * 16) = make_float4(g, g, g, g);
       }
     }
-    if (tid < kC) {
-      float b = 0.f;
-      if (tid < len) {
-        b = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
-        if (a.beta_is_logit) b = sigmoidf_(b);
-      }
-      s_beta[tid] = b;
-    }
   };
 
   int item = blockIdx.x, gid, h, tok0, len;
@@ -356,6 +359,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
     //      registers); L2 norms of the q, k rows (warps 4-7, one row per thread) ----
     if (tid < kD) {  // thread tid scans word tid of the rows (whichever channel it holds)
+      // beta of row tid: loaded here, stored after the scan, so that the scan hides
+      // its latency
+      float bt = 0.f;
+      if (tid < len) bt = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
       float x[kC];
 #pragma unroll
       for (int r = 0; r < kC; ++r) x[r] = G[r * kD + tid];
@@ -367,6 +374,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       }
 #pragma unroll
       for (int r = 0; r < kC; ++r) G[r * kD + tid] = x[r];
+      if (tid < kC) s_beta[tid] = (a.beta_is_logit && tid < len) ? sigmoidf_(bt) : bt;
     } else {
       // one row per thread (q rows 0..63, then k rows): its sixteen 16-byte chunks
       // in an order rotated by the row, so that a warp's loads hit every bank

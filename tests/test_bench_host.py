@@ -50,8 +50,8 @@ def test_algorithmic_accounting():
     assert abs(bench.prefill_bytes() / 1e6 - 718.0) < 0.5
     # decode: 815 MB of traffic per step of 64 x 96 heads
     assert abs(bench.DEC_BYTES_PER_UNIT * 64 * 96 / 1e6 - 815.0) < 1.0
-    # the pages' "about 127,000 FLOPs per token at head dim 128, chunk 64":
-    # the triangle-aware count used here is within 5 % of it
+    # the pages put the cost near 127 thousand FLOPs per token (head dim 128,
+    # chunk 64): the triangle-aware count used here is within 5 % of that
     g = oracle_pins.golden("kda_cost.json")
     per_token = bench.prefill_flops(g["chunk"], T_=1, H_=1, d=g["d"])
     assert abs(per_token / g["flops_per_token_about"] - 1.0) < 0.05
