@@ -1,13 +1,13 @@
 // kda_prefill_tc.cu -- chunked KDA prefill on the tcgen05 tensor cores (sm_103a).
 //
-// The layer is processed in chunks of C = 64 tokens, each split into four
-// 16-token tiles.  Inside a chunk all tokens are handled at once and the chunks
-// follow one another through the state; with log alpha >= -5 the running
-// log-decay changes by less than 80 over a tile, so every decay factor taken
-// relative to a tile boundary lies within e^-80 .. e^80 (inside the bf16 / fp32
-// exponent range) and every tile, the diagonal ones included, is a dense
-// tensor-core product ("Kimi K3's hybrid block, from first principles", section
-// "From linear attention to the delta rule").  Three kernels per call:
+// The layer is processed in chunks of C = 64 tokens.  Inside a chunk all tokens
+// are handled at once and the chunks follow one another through the state
+// ("Kimi K3's hybrid block, from first principles", section "From linear
+// attention to the delta rule").  With log alpha >= -5 the running log-decay
+// moves by less than 80 (116 in log2) over 16 tokens, so decay factors taken
+// about a row 16 tokens away stay inside the bf16 / fp32 exponent range, and
+// every block of the chunk, the diagonal ones included, is a dense tensor-core
+// product.  Three kernels per call:
 //
 //   1. chunk_base_kernel   prefix sum of chunks per sequence (varlen support).
 //   2. prep_kernel         one CTA per (chunk, head), all chunks in parallel:
@@ -34,8 +34,8 @@
 //   A = Diag(beta) strictly_lower(K~ K-^T),  P = incl_lower(Q~ K-^T)   (K~ = G k,
 //   K- = k / G, Q~ = G q, K^ = (G_C / G) k), T = (I + A)^-1 Diag(beta),
 //   W = T K~, U~ = T V, U = U~ - W S, O = Q~ S + P U, S <- Diag(G_C) S + K^^T U.
-// For the Gram matrices the 1/G factors are taken relative to the end of the
-// column's own 16-token tile, so every factor is within e^-80 .. e^80.
+// For the Gram matrices both factors are taken about the middle row of the
+// row's 32-token span, so every factor is within 2^-116 .. 2^116.
 // V, K~ and K^ enter their products as MN-major operands (64-channel blocks of
 // token rows), so every one of them is produced row by row, like the inputs.
 //
@@ -72,10 +72,8 @@ constexpr int kWsParts = 5;
 __constant__ uint32_t kWsPartOff[kWsParts] = {kWsUt, kWsWQ, kWsKh, kWsP, kWsGam};
 __constant__ uint32_t kWsPartLen[kWsParts] = {16384, 32768, 16384, 8192, 512};
 
-constexpr uint32_t kIdF16Bf16 = idesc_f16(128, 16, true);   // Gram: M128 N16 bf16
-constexpr uint32_t kIdGram32 = idesc_f16(128, 32, true);    // Gram: M128 N32 bf16
-// TMEM columns of the Gram per column tile b: [hi.hi | hi.lo | lo.hi], 16 each
-constexpr uint32_t kGramCols = 48;
+constexpr uint32_t kIdGram32 = idesc_f16(128, 32, true);    // Gram span 0: M128 N32 bf16
+constexpr uint32_t kIdGram64 = idesc_f16(128, 64, true);    // Gram span 1: M128 N64 bf16
 constexpr uint32_t kIdF16N64 = idesc_f16(128, 64, false);   // fp16, N = 64
 constexpr uint32_t kIdF16N128 = idesc_f16(128, 128, false); // fp16, N = 128
 constexpr uint32_t kIdKh = idesc_f16(128, 128, false, false, true);  // fp16, N = 128, B MN-major
@@ -166,9 +164,10 @@ constexpr uint32_t kPrepQ = 0;            // q rows, bf16 [64][128] (256 B rows)
 constexpr uint32_t kPrepK = 16384;        // k rows, bf16 [64][128]
 constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
 constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
-//   Gram (per 64-channel half): A hi/lo [128 x 64] bf16 SW128, B hi/lo [16 x 64]
-constexpr uint32_t kPrepAhi = kPrepX, kPrepAlo = kPrepX + 16384;
-constexpr uint32_t kPrepBhi = kPrepX + 32768, kPrepBlo = kPrepX + 34816;
+//   Gram (per 64-channel half): B_0 hi, lo [32 x 64] and B_1 hi, lo [64 x 64],
+//   bf16 K-major SW128
+constexpr uint32_t kPrepB0h = kPrepX, kPrepB0l = kPrepX + 4096;
+constexpr uint32_t kPrepB1h = kPrepX + 8192, kPrepB1l = kPrepX + 16384;
 //   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64] with padded row
 //   strides (no bank conflicts between the rows a warp touches), 4 KB scratch
 constexpr int kAs = 66, kXs = 68;  // row strides (floats) of A and of the inverse
@@ -179,17 +178,18 @@ constexpr uint32_t kPrepY = kPrepInv + kC * kXs * 4;
 constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 //   T as bf16 hi/lo K-major [64 (t)][64 (j)] tiles over the decay rows
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
-// TMEM: Gram D in columns 0..63, then U~^T (64 columns) and W (128 columns)
-constexpr uint32_t kPrepTmemCols = 256, kTdU = 0, kTdW = 64, kTdScratch = 192;
-static_assert(4 * kGramCols <= kPrepTmemCols, "Gram accumulators fit the TMEM allocation");
+// TMEM: the Gram's D_0 (32 columns), D_1 (64) and A (hi, lo for each channel
+// half: 4 x 32); then U~^T (64 columns), W (128) and a 32-column scratch
+constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
+constexpr uint32_t kTdU = 0, kTdW = 64, kTdScratch = 192;
+static_assert(kTdA + 128 <= kPrepTmemCols, "Gram accumulators and A fit the TMEM allocation");
 static_assert(kTdW + 128 <= kTdScratch && kTdScratch + 32 <= kPrepTmemCols, "TMEM scratch");
 constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
 static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
-static_assert(kPrepBlo + 2048 <= kPrepSmall, "Gram operands inside the reused region");
-static_assert(kPrepBlo == kPrepBhi + 2048, "B_lo is rows 16..31 of the N = 32 Gram operand");
+static_assert(kPrepB1l + 8192 <= kPrepSmall, "Gram operands inside the reused region");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
 static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
               "float4 access to the inverse and the scratch");
@@ -216,10 +216,19 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
 // consecutive groups touch consecutive 16-byte words.
 __host__ __device__ constexpr int gpos(int ch) { return ((ch >> 2) & 1) * 64 + (ch >> 3) * 4 + (ch & 3); }
 
-// 8-channel group c of a decay row
-__device__ __forceinline__ void ld8g(const float* row, int c, float (&f)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(row + 4 * c);
-  const float4 b = *reinterpret_cast<const float4*>(row + 64 + 4 * c);
+// The input rows in shared memory (q, k: 16 chunks of 16 bytes; decay: 32) keep
+// chunk j of row r at chunk j ^ (r % 8), so that threads reading the same chunk
+// of eight consecutive rows hit eight different bank groups.
+__host__ __device__ constexpr int rsw(int r, int j) { return j ^ (r & 7); }
+// Float index in the decay rows of float f (as placed by gpos) of row r.
+__host__ __device__ constexpr int gsw(int r, int f) { return r * 128 + (rsw(r, f >> 2) << 2) + (f & 3); }
+
+// 8-channel group c of decay row r
+__device__ __forceinline__ void ld8g(const float* G, int r, int c, float (&f)[8]) {
+  const float* row = G + r * 128;
+  const int p = rsw(r, c);
+  const float4 a = *reinterpret_cast<const float4*>(row + 4 * p);
+  const float4 b = *reinterpret_cast<const float4*>(row + 64 + 4 * p);
   f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       const int rr = r < len ? r : 0;
       const char* src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q) +
                         ((size_t)(tok0 + rr) * H + h) * 256 + (size_t)col16 * 16;
-      cp_async16(smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + col16 * 16), src,
+      cp_async16(smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + rsw(r, col16) * 16), src,
                  r < len ? 16u : 0u);
     }
     if (a.decay_mode == KDA_DECAY_CHANNEL) {  // log alpha rows of 512 B
@@ -331,7 +340,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         const char* src = reinterpret_cast<const char*>(a.log_alpha) +
                           ((size_t)(tok0 + rr) * H + h) * 512 + (size_t)col16 * 16;
         // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
-        cp_async16(smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + (col16 >> 1) * 16), src,
+        cp_async16(smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + rsw(r, col16 >> 1) * 16),
+                   src,
                    r < len ? 16u : 0u);
       }
     }
@@ -358,14 +368,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
     //      registers); L2 norms of the q, k rows (warps 4-7, one row per thread) ----
-    if (tid < kD) {  // thread tid scans word tid of the rows (whichever channel it holds)
+    if (tid < kD) {  // thread tid scans float tid (as placed by gpos) of the rows
       // beta of row tid: loaded here, stored after the scan, so that the scan hides
       // its latency
       float bt = 0.f;
       if (tid < len) bt = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
       float x[kC];
 #pragma unroll
-      for (int r = 0; r < kC; ++r) x[r] = G[r * kD + tid];
+      for (int r = 0; r < kC; ++r) x[r] = G[gsw(r, tid)];
       float run = 0.f;
 #pragma unroll
       for (int r = 0; r < kC; ++r) {
@@ -373,7 +383,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         x[r] = run;
       }
 #pragma unroll
-      for (int r = 0; r < kC; ++r) G[r * kD + tid] = x[r];
+      for (int r = 0; r < kC; ++r) G[gsw(r, tid)] = x[r];
       if (tid < kC) s_beta[tid] = (a.beta_is_logit && tid < len) ? sigmoidf_(bt) : bt;
     } else {
       // one row per thread (q rows 0..63, then k rows): its sixteen 16-byte chunks
@@ -399,111 +409,132 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     }
     __syncthreads();
 
-    // ---- 3. Gram matrices: column tile b, 64-channel half kh at a time ----
-    //   A rows r >= 16b: [k^_r ; q^_r] * 2^(g_r - gend_b);  B rows j in tile b:
-    //   k^_j * 2^(gend_b - g_j); bf16 hi/lo; D[:, 16b..16b+15] += A B^T (3 products).
-    //   Pipelined: a round's operand items are computed into registers while the
-    //   previous round's MMAs still read the operand tiles, then stored.
-#pragma unroll 1
-    for (int round = 0; round < 8; ++round) {
-      const int b = round >> 1, kh = round & 1;
-      const int nA = (kC - 16 * b) * 8;  // A items (row, 8-channel group), then 128 B items
-      // the decay at the end of tile b, for this thread's channel group (every
-      // item of this thread has the same group, 8 kh + tid % 8)
-      float ge[8];
-      ld8g(G + (16 * b + 15) * kD, 8 * kh + (tid & 7), ge);
-      uint4 iv0[3], iv1[3], iv2[3], iv3[3];
-      uint32_t io0[3], io1[3];
-      int kind[3];  // 0: none, 1: A item, 2: B item
+    // ---- 3. Gram matrices over two 32-token spans sp (rows 32 sp .. 32 sp + 31),
+    //   each rescaled about its middle row m = 32 sp + 15: from there the running
+    //   log2-decay moves by at most 16 * 5 * log2(e) < 116, so every factor below
+    //   lies within 2^-116 .. 2^116 (bf16 range).
+    //   A (TMEM, both 64-channel halves): lane r = k^_r 2^(g_r - g_m), lane 64 + r
+    //   = q^_r 2^(g_r - g_m), m the middle row of r's span.
+    //   B_sp (shared memory, one half at a time): rows j < 32 (sp + 1) =
+    //   k^_j 2^(g_m - g_j).
+    //   D_sp = A B_sp^T then holds K~ K-^T and Q~ K-^T on the rows of span sp
+    //   (its other rows, and the columns j > r, are never read); bf16 hi/lo,
+    //   D += A_hi B_hi + A_hi B_lo + A_lo B_hi.
+    fence_after_sync();
+    {
+      // A: lane 32 (warp % 4) + lane, channel half warp / 4 (the TMEM column of a
+      // store is one for the whole warp: every lane takes the same group)
+      const int rho = (warp & 3) * 32 + lane, r = rho & (kC - 1), khA = warp >> 2;
+      const int mr = 32 * (r >> 5) + 15;
+      const uint8_t* xrow = sm + (rho < kC ? kPrepK : kPrepQ) + r * 256;
+      const float inv = rho < kC ? s_invk[r] : s_invq[r];
+      const float2 inv2 = make_float2(inv, inv);
+#pragma unroll 2
+      for (int gi = 0; gi < 8; ++gi) {
+        const int c = 8 * khA + gi;
+        float g8[8], m8[8], xf[8];
+        ld8g(G, r, c, g8);
+        ld8g(G, mr, c, m8);
+        unpack8(*reinterpret_cast<const uint4*>(xrow + rsw(r, c) * 16), xf);
+        uint32_t hi[4], lo[4];
 #pragma unroll
-      for (int s = 0; s < 3; ++s) {
-        const int it = tid + kPrepThreads * s;
-        kind[s] = it < nA ? 1 : (it < nA + 128 ? 2 : 0);
-        if (kind[s] == 1) {
-          const int r = 16 * b + (it >> 3), c8 = it & 7;
-          const int ch = 64 * kh + 8 * c8;
-          float g8[8], kf[8], qf[8];
-          ld8g(G + r * kD, 8 * kh + c8, g8);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
-          const float ik = s_invk[r], iq = s_invq[r];
-          const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
-          uint32_t khi[4], klo[4], qhi[4], qlo[4];
+        for (int u = 0; u < 4; ++u) {
+          const float2 d = sub2(make_float2(g8[2 * u], g8[2 * u + 1]),
+                                make_float2(m8[2 * u], m8[2 * u + 1]));
+          split2v(mul2(make_float2(xf[2 * u], xf[2 * u + 1]),
+                       mul2(make_float2(ex2f(d.x), ex2f(d.y)), inv2)), hi[u], lo[u]);
+        }
+        // channels 8 gi .. +7 of the half are the bf16 pairs in columns 4 gi .. +3
+        const uint32_t col = kTdA + 64 * khA + 4 * gi;
+        tmem_st4(taddr(tmem, (warp & 3) * 32, col), hi[0], hi[1], hi[2], hi[3]);
+        tmem_st4(taddr(tmem, (warp & 3) * 32, col + 32), lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    {
+      // B items of half kh: e = tid + 256 s3 -- span 0 rows for s3 = 0, span 1
+      // rows for s3 = 1, 2 -- each one row j and the 8-channel group tid % 8
+      const int c8 = tid & 7;
+      uint4 vh[3], vl[3];
+      uint32_t vo[3];
+      auto b_items = [&](int kh) {
+        float m0[8], m1[8];
+        ld8g(G, 15, 8 * kh + c8, m0);
+        ld8g(G, 47, 8 * kh + c8, m1);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 d = sub2(make_float2(g8[2 * u], g8[2 * u + 1]),
-                                  make_float2(ge[2 * u], ge[2 * u + 1]));
-            const float2 e = make_float2(ex2f(d.x), ex2f(d.y));
-            split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]), mul2(e, ik2)), khi[u], klo[u]);
-            split2v(mul2(make_float2(qf[2 * u], qf[2 * u + 1]), mul2(e, iq2)), qhi[u], qlo[u]);
-          }
-          iv0[s] = make_uint4(khi[0], khi[1], khi[2], khi[3]);
-          iv1[s] = make_uint4(klo[0], klo[1], klo[2], klo[3]);
-          iv2[s] = make_uint4(qhi[0], qhi[1], qhi[2], qhi[3]);
-          iv3[s] = make_uint4(qlo[0], qlo[1], qlo[2], qlo[3]);
-          io0[s] = sw128_chunk(r, c8, 128);
-          io1[s] = sw128_chunk(64 + r, c8, 128);
-        } else if (kind[s] == 2) {
-          const int e = it - nA, jj = e >> 3, c8 = e & 7;
-          const int j = 16 * b + jj, ch = 64 * kh + 8 * c8;
+        for (int s3 = 0; s3 < 3; ++s3) {
+          const int j = ((tid + kPrepThreads * s3) - (s3 ? kPrepThreads : 0)) >> 3;
           float g8[8], kf[8];
-          ld8g(G + j * kD, 8 * kh + c8, g8);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + ch * 2), kf);
+          ld8g(G, j, 8 * kh + c8, g8);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + rsw(j, 8 * kh + c8) * 16),
+                  kf);
           const float ik = s_invk[j];
           const float2 ik2 = make_float2(ik, ik);
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float2 d = sub2(make_float2(ge[2 * u], ge[2 * u + 1]),
-                                  make_float2(g8[2 * u], g8[2 * u + 1]));
+            const float2 m = s3 ? make_float2(m1[2 * u], m1[2 * u + 1])
+                                : make_float2(m0[2 * u], m0[2 * u + 1]);
+            const float2 d = sub2(m, make_float2(g8[2 * u], g8[2 * u + 1]));
             split2v(mul2(make_float2(kf[2 * u], kf[2 * u + 1]),
                          mul2(make_float2(ex2f(d.x), ex2f(d.y)), ik2)), hi[u], lo[u]);
           }
-          iv0[s] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          iv1[s] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          io0[s] = sw128_chunk(jj, c8, 16);
+          vh[s3] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          vl[s3] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          vo[s3] = (s3 ? kPrepB1h : kPrepB0h) + sw128_chunk(j, c8, 64);
         }
-      }
-      bool waited = true;
-      if (round > 0) {  // the previous round's MMAs must be done reading the tiles
-        waited = mbar_wait(&bar_mma, mma_phase, t.spins);
-        mma_phase ^= 1;
-        fence_after_sync();
-      }
+      };
+      auto b_store = [&]() {
 #pragma unroll
-      for (int s = 0; s < 3; ++s) {
-        if (kind[s] == 1) {
-          *reinterpret_cast<uint4*>(sm + kPrepAhi + io0[s]) = iv0[s];
-          *reinterpret_cast<uint4*>(sm + kPrepAlo + io0[s]) = iv1[s];
-          *reinterpret_cast<uint4*>(sm + kPrepAhi + io1[s]) = iv2[s];
-          *reinterpret_cast<uint4*>(sm + kPrepAlo + io1[s]) = iv3[s];
-        } else if (kind[s] == 2) {
-          *reinterpret_cast<uint4*>(sm + kPrepBhi + io0[s]) = iv0[s];
-          *reinterpret_cast<uint4*>(sm + kPrepBlo + io0[s]) = iv1[s];
+        for (int s3 = 0; s3 < 3; ++s3) {
+          *reinterpret_cast<uint4*>(sm + vo[s3]) = vh[s3];
+          // the lo tile follows its hi tile
+          *reinterpret_cast<uint4*>(sm + vo[s3] + (s3 ? kPrepB1l - kPrepB1h : kPrepB0l - kPrepB0h)) =
+              vl[s3];
         }
+      };
+      auto gram_mma = [&](int kh) {
+        const uint64_t d0h = desc_k_sw128(smem_u32(sm + kPrepB0h), 0);
+        const uint64_t d0l = desc_k_sw128(smem_u32(sm + kPrepB0l), 0);
+        const uint64_t d1h = desc_k_sw128(smem_u32(sm + kPrepB1h), 0);
+        const uint64_t d1l = desc_k_sw128(smem_u32(sm + kPrepB1l), 0);
+        // a K-step of 16 channels: 8 TMEM columns of A, 32 bytes (+2 in the
+        // descriptor's address field) of each B row
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t ah = tmem + kTdA + 64 * kh + 8 * ks, al = ah + 32;
+          const uint32_t acc = (kh | ks) ? 1u : 0u;
+          mma_ts(tmem + kTdD0, ah, d0h + 2 * ks, kIdGram32, acc);
+          mma_ts(tmem + kTdD0, ah, d0l + 2 * ks, kIdGram32, 1u);
+          mma_ts(tmem + kTdD0, al, d0h + 2 * ks, kIdGram32, 1u);
+          mma_ts(tmem + kTdD1, ah, d1h + 2 * ks, kIdGram64, acc);
+          mma_ts(tmem + kTdD1, ah, d1l + 2 * ks, kIdGram64, 1u);
+          mma_ts(tmem + kTdD1, al, d1h + 2 * ks, kIdGram64, 1u);
+        }
+        mma_commit(&bar_mma);
+      };
+      b_items(0);
+      b_store();
+      tmem_wait_st();
+      fence_proxy_async();
+      fence_before_sync();
+      __syncthreads();
+      if (tid == 0) {
+        fence_after_sync();
+        gram_mma(0);
       }
+      // half 1's B rows are computed while half 0's products read the tiles
+      b_items(1);
+      const bool waited = mbar_wait(&bar_mma, mma_phase, t.spins);
+      mma_phase ^= 1;
+      fence_after_sync();
+      b_store();
       fence_proxy_async();
       fence_before_sync();
       ok = __syncthreads_and(waited);
       if (!ok) goto fail;
       if (tid == 0) {
         fence_after_sync();
-        // A_hi against [B_hi; B_lo] (one N = 32 product: the B_lo tile follows the
-        // B_hi tile as its rows 16..31) and A_lo against B_hi: A is read twice per
-        // K-step instead of three times
-        const uint32_t d = tmem + kGramCols * b;
-        const uint32_t ahi = smem_u32(sm + kPrepAhi), alo = smem_u32(sm + kPrepAlo);
-        const uint32_t bhi = smem_u32(sm + kPrepBhi);
-        const uint64_t dahi = desc_k_sw128(ahi, 0), dalo = desc_k_sw128(alo, 0);
-        const uint64_t dbhi = desc_k_sw128(bhi, 0);
-        // a K-step of 16 elements is 32 bytes: +2 in the descriptor's address field
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t acc = (kh | ks) ? 1u : 0u;
-          mma_ss(d, dahi + 2 * ks, dbhi + 2 * ks, kIdGram32, acc);
-          mma_ss(d + 32, dalo + 2 * ks, dbhi + 2 * ks, kIdF16Bf16, acc);
-        }
-        mma_commit(&bar_mma);
+        gram_mma(1);
       }
     }
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
@@ -517,18 +548,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       {
         const int quarter = warp & 3, chalf = warp >> 2;
         const int r = quarter * 32 + lane;
-        uint32_t x[32];  // columns j = 32 chalf .. +31: tiles 2 chalf, 2 chalf + 1
-#pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2) {
-          uint32_t y[32], z[16];
-          const uint32_t col = kGramCols * (2 * chalf + t2);
-          tmem_ld32(taddr(tmem, quarter * 32, col), y);       // hi.hi | hi.lo
-          tmem_ld16(taddr(tmem, quarter * 32, col + 32), z);  // lo.hi
+        // columns j = 32 chalf .. +31 of D_sp, sp = the span of the warp's rows;
+        // span 0 has only j < 32 (the rest of its rows' columns are j > r: zero)
+        const int sp = quarter & 1;
+        uint32_t x[32];
+        if (sp || chalf == 0) {
+          tmem_ld32(taddr(tmem, quarter * 32, (sp ? kTdD1 : kTdD0) + 32 * chalf), x);
           tmem_wait_ld();
+        } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            x[16 * t2 + j] = __float_as_uint(__uint_as_float(y[j]) + __uint_as_float(y[16 + j]) +
-                                             __uint_as_float(z[j]));
+          for (int j = 0; j < 32; ++j) x[j] = 0u;
         }
         if (r < kC) {
           const float br = s_beta[r];
@@ -570,15 +599,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         // K~ of the 8 items waits in TMEM (columns kTdScratch.., this thread's lane)
         // until every read of the k rows is done
         const uint32_t scratch = taddr(tmem, (warp & 3) * 32, kTdScratch);
-        const float* Gl = G + (kC - 1) * kD;
+
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
-          const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15, ch = 8 * c16;
+          const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15;
           float g8[8], gl8[8], kf[8], qf[8];
-          ld8g(G + r * kD, c16, g8);
-          ld8g(Gl, c16, gl8);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + ch * 2), kf);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + ch * 2), qf);
+          ld8g(G, r, c16, g8);
+          ld8g(G, kC - 1, c16, gl8);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + rsw(r, c16) * 16), kf);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + rsw(r, c16) * 16), qf);
           const float ik = s_invk[r], iq = -s_invq[r];
           const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
           uint32_t wk[4], wq[4], wh[4];
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
               make_uint4(wh[0], wh[1], wh[2], wh[3]);
         }
-        reinterpret_cast<float*>(ws + kWsGam)[rt] = ex2f(Gl[gpos(rt)]);
+        reinterpret_cast<float*>(ws + kWsGam)[rt] = ex2f(G[gsw(kC - 1, gpos(rt))]);
         tmem_wait_st();
         named_sync(kBarRow, kPrepHalf);  // every read of the q, k rows is done: they take K~, V
         uint32_t ktl[32];
@@ -793,6 +822,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      fence_before_sync();  // the TMEM reads above before the next item's TMEM writes
       if (w_next >= items) break;
       item = w_next;
       gid = gid_n;
