@@ -72,8 +72,7 @@ constexpr int kWsParts = 5;
 __constant__ uint32_t kWsPartOff[kWsParts] = {kWsUt, kWsWQ, kWsKh, kWsP, kWsGam};
 __constant__ uint32_t kWsPartLen[kWsParts] = {16384, 32768, 16384, 8192, 512};
 
-constexpr uint32_t kIdGram32 = idesc_f16(128, 32, true);    // Gram span 0: M128 N32 bf16
-constexpr uint32_t kIdGram64 = idesc_f16(128, 64, true);    // Gram span 1: M128 N64 bf16
+constexpr uint32_t kIdGram = idesc_f16(128, 96, true);      // Gram: M128 N96 bf16
 constexpr uint32_t kIdF16N64 = idesc_f16(128, 64, false);   // fp16, N = 64
 constexpr uint32_t kIdF16N128 = idesc_f16(128, 128, false); // fp16, N = 128
 constexpr uint32_t kIdKh = idesc_f16(128, 128, false, false, true);  // fp16, N = 128, B MN-major
@@ -164,10 +163,9 @@ constexpr uint32_t kPrepQ = 0;            // q rows, bf16 [64][128] (256 B rows)
 constexpr uint32_t kPrepK = 16384;        // k rows, bf16 [64][128]
 constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
 constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
-//   Gram (per 64-channel half): B_0 hi, lo [32 x 64] and B_1 hi, lo [64 x 64],
-//   bf16 K-major SW128
-constexpr uint32_t kPrepB0h = kPrepX, kPrepB0l = kPrepX + 4096;
-constexpr uint32_t kPrepB1h = kPrepX + 8192, kPrepB1l = kPrepX + 16384;
+//   Gram (per 64-channel half): B = [B_0; B_1] hi and lo, [96 x 64] bf16 K-major
+//   SW128 each (B_0: rows 0..31, B_1: rows 32..95)
+constexpr uint32_t kPrepBh = kPrepX, kPrepBl = kPrepX + 12288;
 //   solve: Diag(beta) strictly_lower(A) and (I + A)^-1, fp32 [64][64] with padded row
 //   strides (no bank conflicts between the rows a warp touches), 4 KB scratch
 constexpr int kAs = 66, kXs = 68;  // row strides (floats) of A and of the inverse
@@ -178,8 +176,8 @@ constexpr uint32_t kPrepY = kPrepInv + kC * kXs * 4;
 constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 //   T as bf16 hi/lo K-major [64 (t)][64 (j)] tiles over the decay rows
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
-// TMEM: the Gram's D_0 (32 columns), D_1 (64) and A (hi, lo for each channel
-// half: 4 x 32); then U~^T (64 columns), W (128) and a 32-column scratch
+// TMEM: the Gram's D = [D_0 | D_1] (32 + 64 columns) and A (hi, lo for each
+// channel half: 4 x 32); then U~^T (64 columns), W (128) and a 32-column scratch
 constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
 constexpr uint32_t kTdU = 0, kTdW = 64, kTdScratch = 192;
 static_assert(kTdA + 128 <= kPrepTmemCols, "Gram accumulators and A fit the TMEM allocation");
@@ -189,7 +187,7 @@ constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-majo
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
 static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
-static_assert(kPrepB1l + 8192 <= kPrepSmall, "Gram operands inside the reused region");
+static_assert(kPrepBl + 12288 <= kPrepSmall, "Gram operands inside the reused region");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
 static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
               "float4 access to the inverse and the scratch");
@@ -415,8 +413,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     //   lies within 2^-116 .. 2^116 (bf16 range).
     //   A (TMEM, both 64-channel halves): lane r = k^_r 2^(g_r - g_m), lane 64 + r
     //   = q^_r 2^(g_r - g_m), m the middle row of r's span.
-    //   B_sp (shared memory, one half at a time): rows j < 32 (sp + 1) =
-    //   k^_j 2^(g_m - g_j).
+    //   B_sp (shared memory, one half at a time, stacked as [B_0; B_1] for one
+    //   N = 96 product): rows j < 32 (sp + 1) = k^_j 2^(g_m - g_j).
     //   D_sp = A B_sp^T then holds K~ K-^T and Q~ K-^T on the rows of span sp
     //   (its other rows, and the columns j > r, are never read); bf16 hi/lo,
     //   D += A_hi B_hi + A_hi B_lo + A_lo B_hi.
@@ -480,35 +478,28 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           }
           vh[s3] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           vl[s3] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          vo[s3] = (s3 ? kPrepB1h : kPrepB0h) + sw128_chunk(j, c8, 64);
+          vo[s3] = sw128_chunk((s3 ? 32 : 0) + j, c8, 96);
         }
       };
       auto b_store = [&]() {
 #pragma unroll
         for (int s3 = 0; s3 < 3; ++s3) {
-          *reinterpret_cast<uint4*>(sm + vo[s3]) = vh[s3];
-          // the lo tile follows its hi tile
-          *reinterpret_cast<uint4*>(sm + vo[s3] + (s3 ? kPrepB1l - kPrepB1h : kPrepB0l - kPrepB0h)) =
-              vl[s3];
+          *reinterpret_cast<uint4*>(sm + kPrepBh + vo[s3]) = vh[s3];
+          *reinterpret_cast<uint4*>(sm + kPrepBl + vo[s3]) = vl[s3];
         }
       };
       auto gram_mma = [&](int kh) {
-        const uint64_t d0h = desc_k_sw128(smem_u32(sm + kPrepB0h), 0);
-        const uint64_t d0l = desc_k_sw128(smem_u32(sm + kPrepB0l), 0);
-        const uint64_t d1h = desc_k_sw128(smem_u32(sm + kPrepB1h), 0);
-        const uint64_t d1l = desc_k_sw128(smem_u32(sm + kPrepB1l), 0);
+        // one product for both spans: D columns 0..31 (D_0) and 32..95 (D_1)
+        const uint64_t dh = desc_k_sw128(smem_u32(sm + kPrepBh), 0);
+        const uint64_t dl = desc_k_sw128(smem_u32(sm + kPrepBl), 0);
         // a K-step of 16 channels: 8 TMEM columns of A, 32 bytes (+2 in the
         // descriptor's address field) of each B row
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t ah = tmem + kTdA + 64 * kh + 8 * ks, al = ah + 32;
-          const uint32_t acc = (kh | ks) ? 1u : 0u;
-          mma_ts(tmem + kTdD0, ah, d0h + 2 * ks, kIdGram32, acc);
-          mma_ts(tmem + kTdD0, ah, d0l + 2 * ks, kIdGram32, 1u);
-          mma_ts(tmem + kTdD0, al, d0h + 2 * ks, kIdGram32, 1u);
-          mma_ts(tmem + kTdD1, ah, d1h + 2 * ks, kIdGram64, acc);
-          mma_ts(tmem + kTdD1, ah, d1l + 2 * ks, kIdGram64, 1u);
-          mma_ts(tmem + kTdD1, al, d1h + 2 * ks, kIdGram64, 1u);
+          mma_ts(tmem + kTdD0, ah, dh + 2 * ks, kIdGram, (kh | ks) ? 1u : 0u);
+          mma_ts(tmem + kTdD0, ah, dl + 2 * ks, kIdGram, 1u);
+          mma_ts(tmem + kTdD0, al, dh + 2 * ks, kIdGram, 1u);
         }
         mma_commit(&bar_mma);
       };
