@@ -157,8 +157,8 @@ __device__ __forceinline__ int find_seq(const int* base, int N, int gid) {
 // thread, so that two CTAs share an SM and hide each other's waits.
 // Shared memory (offsets from a 1024-aligned base):
 constexpr int kPrepThreads = 256;
-constexpr int kPrepHalf = 128;                   // threads per warp group (steps 5 / 6)
-constexpr uint32_t kBarRow = 1, kBarSolve = 2;   // their named barriers
+constexpr int kPrepHalf = 128;                   // threads per warp group (step 6)
+constexpr uint32_t kBarSolve = 2;                // the inverting group's named barrier
 constexpr uint32_t kPrepQ = 0;            // q rows, bf16 [64][128] (256 B rows)
 constexpr uint32_t kPrepK = 16384;        // k rows, bf16 [64][128]
 constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
@@ -177,11 +177,11 @@ constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 //   T as bf16 hi/lo K-major [64 (t)][64 (j)] tiles over the decay rows
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
 // TMEM: the Gram's D = [D_0 | D_1] (32 + 64 columns) and A (hi, lo for each
-// channel half: 4 x 32); then U~^T (64 columns), W (128) and a 32-column scratch
+// channel half: 4 x 32); then U~^T (64 columns) and W (128)
 constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
-constexpr uint32_t kTdU = 0, kTdW = 64, kTdScratch = 192;
+constexpr uint32_t kTdU = 0, kTdW = 64;
 static_assert(kTdA + 128 <= kPrepTmemCols, "Gram accumulators and A fit the TMEM allocation");
-static_assert(kTdW + 128 <= kTdScratch && kTdScratch + 32 <= kPrepTmemCols, "TMEM scratch");
+static_assert(kTdW + 128 <= kPrepTmemCols, "W fits the TMEM allocation");
 constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
@@ -528,10 +528,57 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         gram_mma(1);
       }
     }
+    // ---- 5. row pass, while the Gram's last products run: -Q~ rows, K^ rows and
+    //      G_C straight to the workspace; K~ (fp16) stays in registers until every
+    //      read of the k rows is done.  Item (row r, 8-channel group c16) =
+    //      tid + 256 m ----
+    uint4 kt4[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15;
+      float g8[8], gl8[8], kf[8], qf[8];
+      ld8g(G, r, c16, g8);
+      ld8g(G, kC - 1, c16, gl8);
+      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + rsw(r, c16) * 16), kf);
+      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + rsw(r, c16) * 16), qf);
+      const float ik = s_invk[r], iq = -s_invq[r];
+      const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
+      uint32_t wk[4], wq[4], wh[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 g2 = make_float2(g8[2 * u], g8[2 * u + 1]);
+        const float2 d = sub2(make_float2(gl8[2 * u], gl8[2 * u + 1]), g2);
+        const float2 e2 = make_float2(ex2f(g2.x), ex2f(g2.y));
+        const float2 f2 = make_float2(ex2f(d.x), ex2f(d.y));
+        const float2 k2 = mul2(make_float2(kf[2 * u], kf[2 * u + 1]), ik2);
+        const float2 q2 = mul2(make_float2(qf[2 * u], qf[2 * u + 1]), iq2);
+        const float2 kt2 = mul2(k2, e2), qt2 = mul2(q2, e2), kh2 = mul2(k2, f2);
+        wk[u] = pack_half2(kt2.x, kt2.y);
+        wq[u] = pack_half2(qt2.x, qt2.y);
+        wh[u] = pack_half2(kh2.x, kh2.y);
+      }
+      kt4[m] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+      *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(kC + r, c16, 128)) =
+          make_uint4(wq[0], wq[1], wq[2], wq[3]);
+      *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
+          make_uint4(wh[0], wh[1], wh[2], wh[3]);
+    }
+    if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(G[gsw(kC - 1, gpos(tid))]);
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
     mma_phase ^= 1;
     if (!ok) goto fail;
     fence_after_sync();
+    // every read of the q, k rows is done: they take K~ and the v rows (bf16, by
+    // 16-byte asynchronous copies that land during the solve), both MN-major
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15;
+      *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = kt4[m];
+      const int rr = r < len ? r : 0;
+      cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
+                 v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
+    }
+    cp_async_commit();
 
     {
       // ---- 4. A (lanes 0..63) to shared memory, P (lanes 64..127) to the workspace ----
@@ -576,69 +623,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       fence_before_sync();
       __syncthreads();
 
-      // ---- 5 / 6. Two warp groups in parallel (disjoint data, named barriers):
-      //      warps 4-7 run the row pass, warps 0-3 invert (I + A) ----
+      // ---- 6. X = (I + A)^-1 in fp32: warps 0-3 invert the diagonal 32-blocks
+      //      (named barriers), warps 4-7 clear the blocks above the diagonal ----
       float* X = reinterpret_cast<float*>(sm + kPrepInv);
       float* Y = reinterpret_cast<float*>(sm + kPrepY);
       if (tid >= kPrepHalf) {
-        // ---- 5. row pass: -Q~ rows, K^ rows and G_C straight to the workspace, K~
-        //      (fp16) into the MN-major operand over the k rows; then the v rows, by
-        //      16-byte asynchronous copies (bf16, landing during the solve), into
-        //      the MN-major operand over the q rows.  Row item (row r, 8-channel
-        //      group c16) = rt + 128 m ----
-        const int rt = tid - kPrepHalf;
-        // K~ of the 8 items waits in TMEM (columns kTdScratch.., this thread's lane)
-        // until every read of the k rows is done
-        const uint32_t scratch = taddr(tmem, (warp & 3) * 32, kTdScratch);
-
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15;
-          float g8[8], gl8[8], kf[8], qf[8];
-          ld8g(G, r, c16, g8);
-          ld8g(G, kC - 1, c16, gl8);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + rsw(r, c16) * 16), kf);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + rsw(r, c16) * 16), qf);
-          const float ik = s_invk[r], iq = -s_invq[r];
-          const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
-          uint32_t wk[4], wq[4], wh[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 g2 = make_float2(g8[2 * u], g8[2 * u + 1]);
-            const float2 d = sub2(make_float2(gl8[2 * u], gl8[2 * u + 1]), g2);
-            const float2 e2 = make_float2(ex2f(g2.x), ex2f(g2.y));
-            const float2 f2 = make_float2(ex2f(d.x), ex2f(d.y));
-            const float2 k2 = mul2(make_float2(kf[2 * u], kf[2 * u + 1]), ik2);
-            const float2 q2 = mul2(make_float2(qf[2 * u], qf[2 * u + 1]), iq2);
-            const float2 kt2 = mul2(k2, e2), qt2 = mul2(q2, e2), kh2 = mul2(k2, f2);
-            wk[u] = pack_half2(kt2.x, kt2.y);
-            wq[u] = pack_half2(qt2.x, qt2.y);
-            wh[u] = pack_half2(kh2.x, kh2.y);
-          }
-          tmem_st4(scratch + 4 * m, wk[0], wk[1], wk[2], wk[3]);
-          *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(kC + r, c16, 128)) =
-              make_uint4(wq[0], wq[1], wq[2], wq[3]);
-          *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
-              make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        for (int e = tid - kPrepHalf; e < 6 * 256; e += kPrepHalf) {
+          const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+          const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+          const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+          X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
         }
-        reinterpret_cast<float*>(ws + kWsGam)[rt] = ex2f(G[gsw(kC - 1, gpos(rt))]);
-        tmem_wait_st();
-        named_sync(kBarRow, kPrepHalf);  // every read of the q, k rows is done: they take K~, V
-        uint32_t ktl[32];
-        tmem_ld32(scratch, ktl);
-        tmem_wait_ld();
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int e = rt + kPrepHalf * m, r = e >> 4, c16 = e & 15;
-          *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) =
-              make_uint4(ktl[4 * m], ktl[4 * m + 1], ktl[4 * m + 2], ktl[4 * m + 3]);
-          const int rr = r < len ? r : 0;
-          cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
-                     v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
-        }
-        cp_async_commit();
       } else {
-        // ---- 6. X = (I + A)^-1 by 16 x 16 blocks ----
         if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
           const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update
           float x[16];                                          // rows below: 15-FMA chain)
@@ -651,13 +647,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           }
 #pragma unroll
           for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
-        } else {  // the blocks above the diagonal are zero
-          for (int e = tid - 64; e < 6 * 256; e += kPrepHalf - 64) {
-            const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
-          }
         }
         named_sync(kBarSolve, kPrepHalf);
         // 2 x 2 block inverse at 32 x 32: the lower 16 x 16 block of each diagonal
@@ -693,7 +682,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
               make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
       }
-      __syncthreads();  // the diagonal 32-blocks of X are complete; the row pass is issued
+      __syncthreads();  // the diagonal 32-blocks of X are complete
       // the lower 32-block, X_10 = -X_11 A_10 X_00, by all threads: unit = (row r,
       // 4 columns c4) of the 32 x 32 block
       {  // C1: Z = A_10 X_00
@@ -722,7 +711,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         *reinterpret_cast<float4*>(X + (32 + r) * kXs + c4) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
       }
-      __syncthreads();  // X, the workspace rows, K~ and the v copies are all issued
+      __syncthreads();  // X is complete
 
       // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
       //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
