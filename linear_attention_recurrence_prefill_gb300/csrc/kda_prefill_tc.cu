@@ -176,6 +176,8 @@ constexpr uint32_t kPrepY = kPrepInv + kC * kXs * 4;
 constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 //   T as bf16 hi/lo K-major [64 (t)][64 (j)] tiles over the decay rows
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
+//   U~^T and W staged for their bulk copies to the workspace
+constexpr uint32_t kPrepStU = kPrepX, kPrepStW = kPrepX + 16384;
 // TMEM: the Gram's D = [D_0 | D_1] (32 + 64 columns) and A (hi, lo for each
 // channel half: 4 x 32); then U~^T (64 columns) and W (128)
 constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
@@ -189,6 +191,7 @@ constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment s
 static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
 static_assert(kPrepBl + 12288 <= kPrepSmall, "Gram operands inside the reused region");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
+static_assert(kPrepStW + 16384 <= kPrepSmall, "U~^T and W staging inside the reused region");
 static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
               "float4 access to the inverse and the scratch");
 
@@ -362,6 +365,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   for (;;) {
     uint8_t* ws = ws_block(t, gid, h);
     cp_async_wait_all();
+    if (tid == 0) bulk_wait_read();  // the previous item's results have left region X
     __syncthreads();
 
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
@@ -774,6 +778,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         issue_inputs(h_n, tok0_n, len_n);
       }
       {
+        // U~^T and W go to the free region X in the workspace's byte layout (U~^T:
+        // 16 KB; W: rows 0..63 of each 128-byte K-block of [W; -Q~], 8 KB each)
+        // and leave by three 1-D bulk copies: stored directly, each warp store
+        // would touch 32 different 128-byte lines.
         // warp (quarter, chalf): U~^T rows ch = its TMEM lanes, columns t = 32 chalf ..;
         // W rows t = its lanes mod 64 (both copies), 32-column slab 2 chalf + quarter / 2
         const int quarter = warp & 3, chalf = warp >> 2;
@@ -788,7 +796,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             w[u] = pack_half2(__uint_as_float(x[8 * c8 + 2 * u]), __uint_as_float(x[8 * c8 + 2 * u + 1]));
-          *reinterpret_cast<uint4*>(ws + kWsUt + sw128_chunk(lrow, 4 * chalf + c8, 128)) =
+          *reinterpret_cast<uint4*>(sm + kPrepStU + sw128_chunk(lrow, 4 * chalf + c8, 128)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
         const int tw = lrow & (kC - 1);
@@ -798,11 +806,20 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             w[u] = pack_half2(__uint_as_float(y[8 * c8 + 2 * u]), __uint_as_float(y[8 * c8 + 2 * u + 1]));
-          *reinterpret_cast<uint4*>(ws + kWsWQ + sw128_chunk(tw, 4 * slab + c8, 128)) =
+          const uint32_t o = sw128_chunk(tw, 4 * slab + c8, 128);  // K-block 1 from 16384
+          *reinterpret_cast<uint4*>(sm + kPrepStW + (o < 16384u ? o : o - 8192u)) =
               make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
+      fence_proxy_async();
       fence_before_sync();  // the TMEM reads above before the next item's TMEM writes
+      __syncthreads();
+      if (tid == 0) {
+        bulk_s2g(ws + kWsUt, sm + kPrepStU, 16384);
+        bulk_s2g(ws + kWsWQ, sm + kPrepStW, 8192);
+        bulk_s2g(ws + kWsWQ + 16384, sm + kPrepStW + 8192, 8192);
+        bulk_commit();
+      }
       if (w_next >= items) break;
       item = w_next;
       gid = gid_n;
@@ -821,6 +838,7 @@ fail:
     mbar_wait(&bar_mma, mma_phase, t.spins);
   }
 done:
+  if (tid == 0) bulk_wait_all();
   fence_before_sync();
   __syncthreads();
   fence_after_sync();

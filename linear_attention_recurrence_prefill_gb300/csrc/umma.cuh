@@ -265,6 +265,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until the committed bulk copies have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // 16-byte asynchronous copy global -> shared; `src_bytes` < 16 zero-fills the
 // rest (0 = a zero chunk, nothing read).
