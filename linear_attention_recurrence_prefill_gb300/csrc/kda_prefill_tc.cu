@@ -250,6 +250,23 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return r;
 }
 
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 r;
+  asm("{\n\t.reg .b64 x, y, z, w;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+      "mov.b64 z, {%6, %7};\n\tfma.rn.f32x2 w, x, y, z;\n\tmov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return r;
+}
+// acc += s * x, four lanes in two packed instructions (each lane one fused
+// multiply-add, as the scalar form)
+__device__ __forceinline__ void fma4s(float4& acc, float s, const float4& x) {
+  const float2 s2 = make_float2(s, s);
+  const float2 lo = fma2(s2, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
+  const float2 hi = fma2(s2, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
+  acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 // bf16 hi/lo split of a pair: x ~= hi + lo with ~16 significant bits.
 __device__ __forceinline__ void split2v(float2 x, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x.x, x.y);
@@ -660,13 +677,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         {  // B1: Y_p = A_{2p+1,2p} X_{2p,2p}; unit (p, r, c4)
           const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
           const int i1 = 16 * (2 * p + 1), i0 = 32 * p;
-          const float* arow = Amat + (i1 + r) * kAs + i0;
+          const float2* arow = reinterpret_cast<const float2*>(Amat + (i1 + r) * kAs + i0);
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float am = arow[m];
-            const float4 x4 = *reinterpret_cast<const float4*>(X + (i0 + m) * kXs + i0 + c4);
-            acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+          for (int m2 = 0; m2 < 8; ++m2) {
+            const float2 am = arow[m2];
+            fma4s(acc, am.x, *reinterpret_cast<const float4*>(X + (i0 + 2 * m2) * kXs + i0 + c4));
+            fma4s(acc, am.y, *reinterpret_cast<const float4*>(X + (i0 + 2 * m2 + 1) * kXs + i0 + c4));
           }
           *reinterpret_cast<float4*>(Y + (p << 8) + r * 16 + c4) = acc;
         }
@@ -674,13 +691,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         {  // B2: X_{2p+1,2p} = -X_{2p+1,2p+1} Y_p
           const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
           const int i1 = 16 * (2 * p + 1), i0 = 32 * p;
-          const float* xrow = X + (i1 + r) * kXs + i1;
+          const float4* xrow = reinterpret_cast<const float4*>(X + (i1 + r) * kXs + i1);
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float xm = xrow[m];
-            const float4 y4 = *reinterpret_cast<const float4*>(Y + (p << 8) + m * 16 + c4);
-            acc.x += xm * y4.x; acc.y += xm * y4.y; acc.z += xm * y4.z; acc.w += xm * y4.w;
+          for (int m4 = 0; m4 < 4; ++m4) {
+            const float4 xm = xrow[m4];
+            const float* yb = Y + (p << 8) + 4 * m4 * 16 + c4;
+            fma4s(acc, xm.x, *reinterpret_cast<const float4*>(yb));
+            fma4s(acc, xm.y, *reinterpret_cast<const float4*>(yb + 16));
+            fma4s(acc, xm.z, *reinterpret_cast<const float4*>(yb + 32));
+            fma4s(acc, xm.w, *reinterpret_cast<const float4*>(yb + 48));
           }
           *reinterpret_cast<float4*>(X + (i1 + r) * kXs + i0 + c4) =
               make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
@@ -691,26 +711,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       // 4 columns c4) of the 32 x 32 block
       {  // C1: Z = A_10 X_00
         const int r = tid >> 3, c4 = (tid & 7) * 4;
-        const float* arow = Amat + (32 + r) * kAs;
+        const float2* arow = reinterpret_cast<const float2*>(Amat + (32 + r) * kAs);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int m = 0; m < 32; ++m) {
-          const float am = arow[m];
-          const float4 x4 = *reinterpret_cast<const float4*>(X + m * kXs + c4);
-          acc.x += am * x4.x; acc.y += am * x4.y; acc.z += am * x4.z; acc.w += am * x4.w;
+#pragma unroll 4
+        for (int m2 = 0; m2 < 16; ++m2) {
+          const float2 am = arow[m2];
+          fma4s(acc, am.x, *reinterpret_cast<const float4*>(X + 2 * m2 * kXs + c4));
+          fma4s(acc, am.y, *reinterpret_cast<const float4*>(X + (2 * m2 + 1) * kXs + c4));
         }
         *reinterpret_cast<float4*>(Y + r * 32 + c4) = acc;
       }
       __syncthreads();
       {  // C2: X_10 = -X_11 Z
         const int r = tid >> 3, c4 = (tid & 7) * 4;
-        const float* xrow = X + (32 + r) * kXs + 32;
+        const float4* xrow = reinterpret_cast<const float4*>(X + (32 + r) * kXs + 32);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int m = 0; m < 32; ++m) {
-          const float xm = xrow[m];
-          const float4 z4 = *reinterpret_cast<const float4*>(Y + m * 32 + c4);
-          acc.x += xm * z4.x; acc.y += xm * z4.y; acc.z += xm * z4.z; acc.w += xm * z4.w;
+#pragma unroll 2
+        for (int m4 = 0; m4 < 8; ++m4) {
+          const float4 xm = xrow[m4];
+          const float* zb = Y + 4 * m4 * 32 + c4;
+          fma4s(acc, xm.x, *reinterpret_cast<const float4*>(zb));
+          fma4s(acc, xm.y, *reinterpret_cast<const float4*>(zb + 32));
+          fma4s(acc, xm.z, *reinterpret_cast<const float4*>(zb + 64));
+          fma4s(acc, xm.w, *reinterpret_cast<const float4*>(zb + 96));
         }
         *reinterpret_cast<float4*>(X + (32 + r) * kXs + c4) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
