@@ -73,6 +73,19 @@ def test_k3_shaped_small(impl, T):
     _check(inp, impl, TOL_BF16)
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("la", [-5.0, -7.0, 0.0])
+def test_constant_decay_edges(impl, la):
+    """Every channel at the floor (log alpha = -5, and -7 which the floor clamps to
+    -5): over 16 tokens the running log-decay moves by 80, so the rescaled
+    factors inside a chunk reach e^+-80 on both sides of a row; and no decay at
+    all (log alpha = 0).  T = 200: three full chunks and a ragged tail."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=3, T=200, seed=41)
+    inp.log_alpha = torch.full_like(inp.log_alpha, la)
+    _check(inp, impl, TOL_BF16)
+
+
 @pytest.mark.parametrize("d", [32, 64, 128])
 def test_fp32_path_head_sizes(d):
     dev = _cuda()
