@@ -106,6 +106,31 @@ def test_varlen_small_edges():
         torch.testing.assert_close(S_T[5], inp.S0[5], rtol=0, atol=0)
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+def test_varlen_equals_separate_calls(impl):
+    """Packed sequences give exactly what separate calls on each one give: every
+    chunk restarts at its sequence start, and the kernels do the same arithmetic
+    in the same order either way."""
+    dev = _cuda()
+    lens = [70, 0, 128, 33]
+    inp = inputs.varlen(dev, H=2, lengths=lens)
+    inp.S0 = torch.randn((len(lens), 2, 128, 128), device=dev) * 0.05
+    o, S_T = _gpu_prefill(inp, impl)
+    t0 = 0
+    for n, L in enumerate(lens):
+        sl = lambda x: x[t0:t0 + L].contiguous()  # noqa: E731
+        if L:
+            o1, S1 = kda.kda_prefill(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.log_alpha),
+                                     sl(inp.beta), inp.S0[n:n + 1].contiguous(), N=1,
+                                     gate=sl(inp.gate), impl=impl)
+            torch.cuda.synchronize()
+            assert torch.equal(o[t0:t0 + L], o1), f"sequence {n}: output differs"
+            assert torch.equal(S_T[n:n + 1], S1), f"sequence {n}: state differs"
+        else:
+            assert torch.equal(S_T[n], inp.S0[n])
+        t0 += L
+
+
 def test_no_tokens():
     dev = _cuda()
     S0 = torch.randn((2, 3, 64, 64), device=dev)
