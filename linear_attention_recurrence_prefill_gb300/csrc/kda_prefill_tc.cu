@@ -40,7 +40,7 @@
 // token rows), so every one of them is produced row by row, like the inputs.
 //
 // Precision: the Gram products use a bf16 hi/lo split (hi*hi + hi*lo + lo*hi,
-// ~16 significant bits, bf16 keeps the e^+-80 range); every other product uses
+// ~16 significant bits, bf16 keeps the 2^+-116 range); every other product uses
 // fp16 operands (11 significant bits; all values there are within fp16 range
 // or negligibly small) with fp32 accumulation; the state itself stays fp32.
 #include <stdio.h>
