@@ -131,6 +131,24 @@ def test_varlen_equals_separate_calls(impl):
         t0 += L
 
 
+@pytest.mark.parametrize("impl", IMPLS)
+def test_equal_length_batch(impl):
+    """N = 3 sequences of 100 tokens given as N alone (no cu_seqlens): each
+    sequence's chunks, the last one ragged, are found by arithmetic.  Checked
+    against the oracle, and bit for bit against the same batch with explicit
+    cu_seqlens."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=2, T=300, seed=43)
+    inp.N = 3
+    inp.S0 = torch.randn((3, 2, 128, 128), device=dev) * 0.05
+    o, S_T = _check(inp, impl, TOL_BF16)
+    cu = torch.tensor([0, 100, 200, 300], dtype=torch.int32, device=dev)
+    o2, S2 = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0, cu,
+                             gate=inp.gate, impl=impl)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(S_T, S2)
+
+
 def test_no_tokens():
     dev = _cuda()
     S0 = torch.randn((2, 3, 64, 64), device=dev)
