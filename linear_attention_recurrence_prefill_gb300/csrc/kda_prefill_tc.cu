@@ -1172,15 +1172,22 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       named_sync(kBarEpi, kChEpi);
       if (et == 0) mbar_arrive(&bar_oe[i & 1]);  // O^T(i) is out of TMEM: the buffer is free
       // pass 1: sum of squares of the row; pass 2: outputs, 8 channels at a time
+      // the row's 32 values of this thread stay in registers for both passes
       const float* erow = E + er * kEStride;
-      float ss = 0.f;
-#pragma unroll
+      float4 ev[8];
+      float2 ss2 = make_float2(0.f, 0.f);  // packed f32x2 arithmetic: fewer issue slots
+#pragma unroll                            // taken from the state warps
       for (int c = 0; c < 4; ++c) {
         const float4 v0 = *reinterpret_cast<const float4*>(erow + 8 * (eq + 4 * c));
         const float4 v1 = *reinterpret_cast<const float4*>(erow + 8 * (eq + 4 * c) + 4);
-        ss += v0.x * v0.x + v0.y * v0.y + v0.z * v0.z + v0.w * v0.w;
-        ss += v1.x * v1.x + v1.y * v1.y + v1.z * v1.z + v1.w * v1.w;
+        ev[2 * c] = v0;
+        ev[2 * c + 1] = v1;
+        ss2 = fma2(make_float2(v0.x, v0.y), make_float2(v0.x, v0.y), ss2);
+        ss2 = fma2(make_float2(v0.z, v0.w), make_float2(v0.z, v0.w), ss2);
+        ss2 = fma2(make_float2(v1.x, v1.y), make_float2(v1.x, v1.y), ss2);
+        ss2 = fma2(make_float2(v1.z, v1.w), make_float2(v1.z, v1.w), ss2);
       }
+      float ss = ss2.x + ss2.y;
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       const float inv = gate ? rsqrtf(ss * (1.0f / kD) + a.eps_norm) : 1.f;
@@ -1190,17 +1197,19 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int q = eq + 4 * c;
-          const float4 v0 = *reinterpret_cast<const float4*>(erow + 8 * q);
-          const float4 v1 = *reinterpret_cast<const float4*>(erow + 8 * q + 4);
+          const float4 v0 = ev[2 * c], v1 = ev[2 * c + 1];
           float y[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
           if (gate) {
             const uint4 graw = *reinterpret_cast<const uint4*>(sm + gate_slot(i, c));
             const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw);
+            const float2 hinv2 = make_float2(hinv, hinv);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float2 gf = __bfloat1622float2(g2[u]);
-              y[2 * u] *= fmaf(tanh_approx(0.5f * gf.x), hinv, hinv);
-              y[2 * u + 1] *= fmaf(tanh_approx(0.5f * gf.y), hinv, hinv);
+              const float2 gh = mul2(__bfloat1622float2(g2[u]), make_float2(0.5f, 0.5f));
+              const float2 sg = fma2(make_float2(tanh_approx(gh.x), tanh_approx(gh.y)), hinv2, hinv2);
+              const float2 yy = mul2(make_float2(y[2 * u], y[2 * u + 1]), sg);
+              y[2 * u] = yy.x;
+              y[2 * u + 1] = yy.y;
             }
             if (a.norm_weight) {
               const float4* w4 = reinterpret_cast<const float4*>(a.norm_weight + 8 * q);
