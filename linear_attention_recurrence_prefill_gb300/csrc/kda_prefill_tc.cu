@@ -178,6 +178,9 @@ constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
 //   U~^T and W staged for their bulk copies to the workspace
 constexpr uint32_t kPrepStU = kPrepX, kPrepStW = kPrepX + 16384;
+//   Z = A_10 X_00 of the inverse (fp32 [32][32]) over the decay rows, which the
+//   row pass has finished reading and the T tiles take only later
+constexpr uint32_t kPrepZ = kPrepG;
 // TMEM: the Gram's D = [D_0 | D_1] (32 + 64 columns) and A (hi, lo for each
 // channel half: 4 x 32); then U~^T (64 columns) and W (128)
 constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
@@ -644,10 +647,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       fence_before_sync();
       __syncthreads();
 
-      // ---- 6. X = (I + A)^-1 in fp32: warps 0-3 invert the diagonal 32-blocks
-      //      (named barriers), warps 4-7 clear the blocks above the diagonal ----
+      // ---- 6. X = (I + A)^-1 in fp32: warps 0-1 invert the diagonal 16-blocks
+      //      while warps 4-7 clear the blocks above the diagonal; then warps 0-3
+      //      complete the diagonal 32-blocks (named barriers) while warps 4-7 form
+      //      the parts of Z = A_10 X_00 that need only the diagonal 16-blocks ----
       float* X = reinterpret_cast<float*>(sm + kPrepInv);
       float* Y = reinterpret_cast<float*>(sm + kPrepY);
+      float* Z = reinterpret_cast<float*>(sm + kPrepZ);
       if (tid >= kPrepHalf) {
         for (int e = tid - kPrepHalf; e < 6 * 256; e += kPrepHalf) {
           const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
@@ -655,8 +661,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
           X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
         }
-      } else {
-        if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
+      } else if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
           const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update
           float x[16];                                          // rows below: 15-FMA chain)
 #pragma unroll
@@ -668,8 +673,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           }
 #pragma unroll
           for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
+      }
+      __syncthreads();  // the diagonal 16-blocks are complete, the upper blocks clear
+      if (tid >= kPrepHalf) {
+        // Z = A_10 X_00 (A_10: A rows 32..63, columns 0..31) without its x10 term:
+        // columns 16..31 in full (A_10[:, 16..31] x11), columns 0..15 as far as
+        // A_10[:, 0..15] x00.  Unit = (row r, 4 columns c4), two per thread.
+        for (int e = tid - kPrepHalf; e < 32 * 8; e += kPrepHalf) {
+          const int r = e >> 3, c4 = (e & 7) * 4, b = c4 >> 4;
+          const float2* arow = reinterpret_cast<const float2*>(Amat + (32 + r) * kAs + 16 * b);
+          const float* xb = X + 16 * b * kXs + c4;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int m2 = 0; m2 < 8; ++m2) {
+            const float2 am = arow[m2];
+            fma4s(acc, am.x, *reinterpret_cast<const float4*>(xb + 2 * m2 * kXs));
+            fma4s(acc, am.y, *reinterpret_cast<const float4*>(xb + (2 * m2 + 1) * kXs));
+          }
+          *reinterpret_cast<float4*>(Z + r * 32 + c4) = acc;
         }
-        named_sync(kBarSolve, kPrepHalf);
+      } else {
         // 2 x 2 block inverse at 32 x 32: the lower 16 x 16 block of each diagonal
         // 32-block, X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (B1, B2);
         // the lower 32-block follows below with all threads (C1, C2).  Each unit
@@ -707,19 +730,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         }
       }
       __syncthreads();  // the diagonal 32-blocks of X are complete
-      // the lower 32-block, X_10 = -X_11 A_10 X_00, by all threads: unit = (row r,
-      // 4 columns c4) of the 32 x 32 block
-      {  // C1: Z = A_10 X_00
-        const int r = tid >> 3, c4 = (tid & 7) * 4;
-        const float2* arow = reinterpret_cast<const float2*>(Amat + (32 + r) * kAs);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int m2 = 0; m2 < 16; ++m2) {
+      // the lower 32-block, X_10 = -X_11 A_10 X_00: unit = (row r, 4 columns c4)
+      if (tid < kPrepHalf) {  // Z[:, 0..15] += A_10[:, 16..31] x10 (the same order of
+        const int r = tid >> 2, c4 = (tid & 3) * 4;  // terms as one pass over m)
+        const float2* arow = reinterpret_cast<const float2*>(Amat + (32 + r) * kAs + 16);
+        const float* xb = X + 16 * kXs + c4;
+        float4 acc = *reinterpret_cast<const float4*>(Z + r * 32 + c4);
+#pragma unroll
+        for (int m2 = 0; m2 < 8; ++m2) {
           const float2 am = arow[m2];
-          fma4s(acc, am.x, *reinterpret_cast<const float4*>(X + 2 * m2 * kXs + c4));
-          fma4s(acc, am.y, *reinterpret_cast<const float4*>(X + (2 * m2 + 1) * kXs + c4));
+          fma4s(acc, am.x, *reinterpret_cast<const float4*>(xb + 2 * m2 * kXs));
+          fma4s(acc, am.y, *reinterpret_cast<const float4*>(xb + (2 * m2 + 1) * kXs));
         }
-        *reinterpret_cast<float4*>(Y + r * 32 + c4) = acc;
+        *reinterpret_cast<float4*>(Z + r * 32 + c4) = acc;
       }
       __syncthreads();
       {  // C2: X_10 = -X_11 Z
@@ -729,7 +752,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll 2
         for (int m4 = 0; m4 < 8; ++m4) {
           const float4 xm = xrow[m4];
-          const float* zb = Y + 4 * m4 * 32 + c4;
+          const float* zb = Z + 4 * m4 * 32 + c4;
           fma4s(acc, xm.x, *reinterpret_cast<const float4*>(zb));
           fma4s(acc, xm.y, *reinterpret_cast<const float4*>(zb + 32));
           fma4s(acc, xm.z, *reinterpret_cast<const float4*>(zb + 64));
