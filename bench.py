@@ -59,7 +59,7 @@ def prefill_flops(chunk: int, T_=T, H_=H, d=D):
 TRAFFIC: dict[str, float | None] = {
     # profiles/prep_kernel_k3_prefill.md, profiles/chain_kernel_k3_prefill.md
     # (dram read + write of one launch)
-    "prep_kernel": 504.620544e6 + 407.611648e6,
+    "prep_kernel": 504.551424e6 + 407.481856e6,
     "chain_kernel": 563.14752e6 + 87.442688e6,
     # profiles/decode_kernel_k3_decode.md
     "decode_kernel<128,bf16>": 410.566656e6 + 343.659776e6,
