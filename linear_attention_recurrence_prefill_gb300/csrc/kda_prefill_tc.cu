@@ -10,8 +10,8 @@
 // product.  Three kernels per call:
 //
 //   1. chunk_base_kernel   prefix sum of chunks per sequence (varlen support).
-//   2. prep_kernel         one CTA per (chunk, head), all chunks in parallel:
-//                          prologue (L2 norm, beta, log-decay floor and running
+//   2. prep_kernel         persistent, two CTAs per SM walking the (chunk, head)
+//                          items, all independent; per item: prologue (L2 norm, beta, log-decay floor and running
 //                          sum), the decay-rescaled Gram matrices A and P on the
 //                          tensor cores (bf16 hi/lo split, three products, fp32
 //                          accumulation in TMEM), the unit-lower-triangular solve
