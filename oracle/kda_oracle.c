@@ -66,9 +66,24 @@ enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
 /* Widen element i of a typed buffer to double (exact for all three types). */
 static double load_elem(const void* p, int dtype, size_t i) {
   if (dtype == ORC_F64) return ((const double*)p)[i];
+#if KDA_ORACLE_MUTATION == 11
+  if (dtype == ORC_F32) { /* planted mistake: fp32 cut to its upper 16 bits */
+    float f32 = ((const float*)p)[i];
+    uint32_t b32;
+    memcpy(&b32, &f32, sizeof b32);
+    b32 &= 0xFFFF0000u;
+    memcpy(&f32, &b32, sizeof f32);
+    return (double)f32;
+  }
+#else
   if (dtype == ORC_F32) return (double)((const float*)p)[i];
+#endif
   /* bf16: the upper 16 bits of an IEEE binary32 pattern */
+#if KDA_ORACLE_MUTATION == 10
+  uint32_t bits = ((uint32_t)((const uint16_t*)p)[i]) << 15; /* planted: wrong shift */
+#else
   uint32_t bits = ((uint32_t)((const uint16_t*)p)[i]) << 16;
+#endif
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;

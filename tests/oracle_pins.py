@@ -353,6 +353,117 @@ def pin_gated_rmsnorm(orc):
     np.testing.assert_allclose(y1[:, 0], y[:, 1], rtol=1e-14)
 
 
+# ---------------------------------------------------------------- input widening
+# bf16 bit patterns with their values written out from the IEEE binary32 layout
+# (a bf16 value is the upper half of a binary32 pattern)
+BF16_KNOWN = [
+    (0x3F80, 1.0),
+    (0xC0A0, -5.0),
+    (0x3FC0, 1.5),
+    (0x0001, 2.0 ** -133),                         # smallest positive subnormal
+    (0x8000, -0.0),
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127),      # largest finite
+    (0x4049, 3.140625),
+    (0xBE80, -0.25),
+]
+
+
+def _bf16_tensor(bits, shape=None):
+    import torch
+    t = torch.from_numpy(np.array(bits, dtype=np.uint16).view(np.int16).copy()).view(
+        torch.bfloat16)
+    return t.reshape(shape) if shape is not None else t
+
+
+def _bf16_values(t):
+    """fp64 values of a bf16 tensor by the library's own conversion."""
+    import torch
+    return t.to(torch.float64).numpy()
+
+
+def pin_input_widening(orc):
+    """Inputs stored as bf16 (raw 16-bit patterns) or fp32 are widened exactly.
+
+    Known bf16 patterns pass through exact identity paths of the recurrence
+    (S0 = I with beta = 0 returns q; one write with beta = 1 returns v, k and
+    beta; the fade of S0 = I returns exp of the clamped log alpha), and through
+    the gate of the RMSNorm epilogue.  Random bf16 and fp32 inputs give results
+    bit-identical to the fp64 run on the same values, for the prefill, the
+    decode step and the gate."""
+    import torch
+    d = len(BF16_KNOWN)
+    bits = [b for b, _ in BF16_KNOWN]
+    vals = np.array([x for _, x in BF16_KNOWN])
+    row = _bf16_tensor(bits, (1, 1, d))
+    eye = np.eye(d)
+    z = lambda *s: torch.zeros(s, dtype=torch.bfloat16)  # noqa: E731
+    one_hot = lambda c, s: _bf16_tensor([0x3F80 if i == c else 0 for i in range(d)], s)  # noqa: E731
+    kw = dict(l2norm_qk=False, eps_l2=0.0)
+    # q: S0 = I, beta = 0, no decay -> o = q
+    o, _ = orc.prefill(row, z(1, 1, d), z(1, 1, d), np.zeros((1, 1, d)), z(1, 1),
+                       eye[None, None], **kw)
+    np.testing.assert_array_equal(o[0, 0], vals)
+    # v: S0 = 0, beta = 1, k = q = e_0 -> o = v
+    e0 = one_hot(0, (1, 1, d))
+    o, S = orc.prefill(e0, e0, row, np.zeros((1, 1, d)), _bf16_tensor([0x3F80], (1, 1)), **kw)
+    np.testing.assert_array_equal(o[0, 0], vals)
+    np.testing.assert_array_equal(S[0, 0, 0], vals)
+    # k: head h reads channel h of the key just written (v = e_0): o[h, 0] = k_h
+    H = d
+    krow = torch.cat([row] * H, dim=1)
+    qh = torch.cat([one_hot(h, (1, 1, d)) for h in range(H)], dim=1)
+    vh = torch.cat([e0] * H, dim=1)
+    o, _ = orc.prefill(qh, krow, vh, np.zeros((1, H, d)), _bf16_tensor([0x3F80] * H, (1, H)),
+                       **kw)
+    np.testing.assert_array_equal(o[0, :, 0], vals)
+    # beta: S0 = 0, k = q = v = e_0 -> o_0 = beta (one head per pattern)
+    e0h = torch.cat([e0] * H, dim=1)
+    o, _ = orc.prefill(e0h, e0h, e0h, np.zeros((1, H, d)), _bf16_tensor(bits, (1, H)), **kw)
+    np.testing.assert_array_equal(o[0, :, 0], vals)
+    # log alpha (bf16 and fp32 storage): S0 = I, beta = 0, head h reads channel h
+    la32 = np.array([-5.0, -0.25, -1e-4, -3.3, 0.0, -4.99, -0.001, -2.0], dtype=np.float32)
+    for la, la64 in ((row.expand(1, H, d).contiguous(), vals),
+                     (np.broadcast_to(la32, (1, H, d)).copy(), la32.astype(np.float64))):
+        S0 = np.broadcast_to(eye, (1, H, d, d)).copy()
+        o, _ = orc.prefill(qh, z(1, H, d), z(1, H, d), la, z(1, H), S0, **kw)
+        want = np.exp(np.minimum(np.maximum(la64, -5.0), 0.0))
+        np.testing.assert_array_equal(np.diagonal(o[0]), want)
+    # the gate: y = sigmoid(g) for a constant unit output
+    y = orc.gated_rmsnorm(np.ones((1, 1, d)), row, eps=0.0)
+    np.testing.assert_allclose(y[0, 0], 1.0 / (1.0 + np.exp(-vals)), rtol=1e-15, atol=0)
+    # random inputs: bf16 / fp32 storage == fp64 of the same values, bit for bit
+    r = _rng(37)
+    T, H2, dd = 9, 3, 8
+    g = torch.Generator().manual_seed(37)
+    qb, kb, vb = (torch.randn((T, H2, dd), generator=g).to(torch.bfloat16) for _ in range(3))
+    bb = torch.rand((T, H2), generator=g).to(torch.bfloat16)
+    lab = (-6.0 * torch.rand((T, H2, dd), generator=g)).to(torch.bfloat16)
+    la_f32 = r.uniform(-6.0, 0.1, size=(T, H2, dd)).astype(np.float32)
+    S0 = r.normal(size=(1, H2, dd, dd))
+    for la_in, la_ref in ((lab, _bf16_values(lab)), (la_f32, la_f32.astype(np.float64))):
+        o1, s1 = orc.prefill(qb, kb, vb, la_in, bb, S0)
+        o2, s2 = orc.prefill(_bf16_values(qb), _bf16_values(kb), _bf16_values(vb), la_ref,
+                             _bf16_values(bb), S0)
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(s1, s2)
+        d1, n1 = orc.decode_step(qb[:1], kb[:1], vb[:1], la_in[:1], bb[:1], S0)
+        d2, n2 = orc.decode_step(_bf16_values(qb[:1]), _bf16_values(kb[:1]), _bf16_values(vb[:1]),
+                                 la_ref[:1], _bf16_values(bb[:1]), S0)
+        np.testing.assert_array_equal(d1, d2)
+        np.testing.assert_array_equal(n1, n2)
+    q32, k32, v32 = (r.normal(size=(T, H2, dd)).astype(np.float32) for _ in range(3))
+    b32 = r.uniform(0, 1, size=(T, H2)).astype(np.float32)
+    o1, s1 = orc.prefill(q32, k32, v32, la_f32, b32, S0)
+    o2, s2 = orc.prefill(q32.astype(np.float64), k32.astype(np.float64), v32.astype(np.float64),
+                         la_f32.astype(np.float64), b32.astype(np.float64), S0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(s1, s2)
+    gb = torch.randn((T, H2, dd), generator=g).to(torch.bfloat16)
+    g32 = r.normal(size=(T, H2, dd)).astype(np.float32)
+    for gin, gref in ((gb, _bf16_values(gb)), (g32, g32.astype(np.float64))):
+        np.testing.assert_array_equal(orc.gated_rmsnorm(o1, gin), orc.gated_rmsnorm(o1, gref))
+
+
 ALL_PINS = [
     pin_brute_force,
     pin_overwrite,
@@ -365,4 +476,5 @@ ALL_PINS = [
     pin_beta_logit,
     pin_split_and_decode,
     pin_gated_rmsnorm,
+    pin_input_widening,
 ]

@@ -4,7 +4,9 @@
 mathematics.  The faithful build must pass every pin; each build with a planted
 mistake (a dropped fade, a read before the write, a wrong sign, a wrong index,
 a dropped beta, a missing floor, the fade in the wrong place, a missing key
-normalisation, the wrong probe vector) must fail at least one of them.
+normalisation, the wrong probe vector, a wrong widening of bf16 or fp32
+inputs) must fail at least one of them.  A marshalling mistake on the Python
+side (bf16 passed through float16) is planted the same way.
 """
 import os
 
@@ -24,6 +26,8 @@ MUTATIONS = {
     7: "fade after the write",
     8: "key not normalised",
     9: "state probed with the query",
+    10: "bf16 input widened with the wrong shift",
+    11: "fp32 input cut to bf16",
 }
 
 
@@ -45,6 +49,29 @@ def test_pins_catch_planted_mistake(tmp_path, m):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught planted mistake {m} ({MUTATIONS[m]})"
+
+
+def test_pins_catch_bf16_marshalled_as_float16(orc, monkeypatch):
+    """bf16 tensors handed over as float16 values (a plausible marshalling slip
+    in the front-end) lose range and precision; the widening pin sees it."""
+    import numpy as np
+    import torch
+
+    from oracle import oracle as front
+
+    good = front._as_buffer
+
+    def wrong(x):
+        if isinstance(x, torch.Tensor) and x.dtype == torch.bfloat16:
+            return x.to(torch.float16).to(torch.float32).numpy(), front._F32
+        return good(x)
+
+    monkeypatch.setattr(front, "_as_buffer", wrong)
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_input_widening(orc)
+    monkeypatch.setattr(front, "_as_buffer", good)
+    oracle_pins.pin_input_widening(orc)
+    assert np.isfinite(good(torch.zeros(2, dtype=torch.bfloat16))[0]).all()
 
 
 def test_state_sizes_golden():
