@@ -206,15 +206,23 @@ int kda_gated_rmsnorm(const void* o, const void* gate, const float* w, void* y, 
  * Arguments, layouts and results are those of kda_prefill, except that
  * opt->workspace is ignored: the scratch is a fixed array of
  * KDA_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads
- * it until the process exits.  Only bf16 with d_k = d_v = 128 is accepted
- * (KDA_ERR_UNSUPPORTED otherwise), and sizes whose scratch
- * (kda_prefill_workspace_size) exceeds the array are refused with
- * KDA_ERR_WORKSPACE before anything is launched.  Nothing is allocated.
+ * it until the process exits.  Errors, all returned before anything is
+ * launched:
+ *   - the argument checks of kda_prefill come first, with its status codes
+ *     (KDA_ERR_ARG, _SHAPE, _DTYPE, _ALIGN, ...);
+ *   - KDA_ERR_UNSUPPORTED for anything the tensor-core path does not take:
+ *     opt->impl other than KDA_IMPL_AUTO / KDA_IMPL_TC, opt->chunk other than
+ *     0 / 64, fp32 data, or d_k = d_v other than 128;
+ *   - KDA_ERR_WORKSPACE for sizes whose scratch (kda_prefill_workspace_size)
+ *     exceeds the array.
+ * Nothing is allocated.
  *
- * The first call on a device looks up the array's device address; make that
- * first call before any stream capture.  All calls share the one array, so
- * calls that can overlap on the GPU (different streams, or other threads)
- * race: order them, e.g. on one stream.  No state carries over between calls.
+ * The first call on a device looks up the array's device address (again after
+ * the device's context is replaced, e.g. by a device reset, since the array
+ * then lives at a new address); make that first call before any stream
+ * capture.  All calls share the one array, so calls that can overlap on the
+ * GPU (different streams, or other threads) race: order them, e.g. on one
+ * stream.  No state carries over between calls.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (64u << 20)
 int kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* log_alpha,

@@ -1,7 +1,10 @@
 // kda_api.cu -- the C ABI of libkda.so: argument checks, path selection and
 // the device status word.  Every check runs on the host before anything is
 // enqueued; a rejected call launches nothing.
+#include <cuda.h>
 #include <string.h>
+
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
@@ -11,15 +14,48 @@ namespace kda {
 // Written by device code when a bounded wait gives up (KDA_ERR_TIMEOUT).
 __device__ int g_status_word = 0;
 
+unsigned long long current_context_id() {
+  // The driver's context queries, reached through the runtime so that the
+  // library needs no link against the driver library.
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 int* status_word() {
+  // looked up once per (device, context): a device reset makes a new context,
+  // in which the word has a new address
+  static std::mutex m;
+  static unsigned long long ctx_of[64] = {0};
   static int* cached[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cached[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    cached[dev] = static_cast<int*>(p);
-  }
+  const unsigned long long id = current_context_id();
+  std::lock_guard<std::mutex> g(m);
+  if (id != 0 && ctx_of[dev] == id && cached[dev]) return cached[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess || !p) return nullptr;
+  cached[dev] = static_cast<int*>(p);
+  ctx_of[dev] = current_context_id();
   return cached[dev];
 }
 
@@ -75,6 +111,53 @@ int prefill_path(const kda_options* o, int d, int dtype) {
 }
 
 }  // namespace
+
+namespace kda {
+
+int check_prefill(const void* q, const void* k, const void* v, const float* log_alpha,
+                  const void* beta, const float* S0, const int32_t* cu_seqlens, int N,
+                  const void* o, const float* S_T, int T_total, int H, int d_k, int d_v,
+                  int dtype, const kda_options* op, int* path_out, int* snap_slots_out) {
+  if (N < 1 || H < 1 || T_total < 0) return KDA_ERR_SHAPE;
+  // token arrays may be NULL only when there are no tokens
+  if (!S_T || (T_total > 0 && (!q || !k || !v || !log_alpha_ok(log_alpha, op->decay_mode) ||
+                               !beta || !o)))
+    return KDA_ERR_ARG;
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
+  if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
+  if (!cu_seqlens && (T_total % N) != 0) return KDA_ERR_SHAPE;
+  if (op->max_seqlen < 0 || op->max_seqlen > T_total) return KDA_ERR_SHAPE;
+  if (op->chunk != 0 && op->chunk != 16 && op->chunk != 64) return KDA_ERR_ARG;
+  const void* ptrs[] = {q, k, v, o, S_T};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
+  if (!log_alpha_aligned(log_alpha, op->decay_mode)) return KDA_ERR_ALIGN;
+  if (beta && !beta_aligned(beta, dtype)) return KDA_ERR_ALIGN;
+  if ((S0 && !aligned16(S0)) || (cu_seqlens && !aligned16(cu_seqlens))) return KDA_ERR_ALIGN;
+  int rc = check_common_opts(op);
+  if (rc != KDA_OK) return rc;
+  // 64-bit extents: every index below 2^62
+  const long long tok_elems = (long long)T_total * H * d_k;
+  if (tok_elems < 0) return KDA_ERR_SHAPE;
+  // state snapshots every snapshot_every tokens (a multiple of the chunk)
+  int snap_slots = 0;
+  if (op->snapshot_every < 0 || (op->snapshot_every > 0 && op->snapshot_every % 64 != 0))
+    return KDA_ERR_ARG;
+  if (op->snapshot_every > 0) {
+    if (!op->snapshots) return KDA_ERR_ARG;
+    if (!aligned16(op->snapshots)) return KDA_ERR_ALIGN;
+    const int L = op->max_seqlen > 0 ? op->max_seqlen : (cu_seqlens ? T_total : T_total / N);
+    snap_slots = L / op->snapshot_every;
+  }
+  const int path = prefill_path(op, d_k, dtype);
+  if (path < 0) return KDA_ERR_UNSUPPORTED;
+  if (path == KDA_IMPL_SIMT && op->chunk == 64) return KDA_ERR_UNSUPPORTED;
+  if (path_out) *path_out = path;
+  if (snap_slots_out) *snap_slots_out = snap_slots;
+  return KDA_OK;
+}
+
+}  // namespace kda
 
 extern "C" {
 
@@ -142,41 +225,10 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
                 const kda_options* opt, kda_stream_t stream) {
   kda_options def;
   const kda_options* op = opts_or_default(opt, &def);
-  if (N < 1 || H < 1 || T_total < 0) return KDA_ERR_SHAPE;
-  // token arrays may be NULL only when there are no tokens
-  if (!S_T || (T_total > 0 && (!q || !k || !v || !log_alpha_ok(log_alpha, op->decay_mode) ||
-                               !beta || !o)))
-    return KDA_ERR_ARG;
-  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_DTYPE;
-  if (d_k != d_v || !supported_d(d_k)) return KDA_ERR_UNSUPPORTED;
-  if (!cu_seqlens && (T_total % N) != 0) return KDA_ERR_SHAPE;
-  if (op->max_seqlen < 0 || op->max_seqlen > T_total) return KDA_ERR_SHAPE;
-  if (op->chunk != 0 && op->chunk != 16 && op->chunk != 64) return KDA_ERR_ARG;
-  const void* ptrs[] = {q, k, v, o, S_T};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return KDA_ERR_ALIGN;
-  if (!log_alpha_aligned(log_alpha, op->decay_mode)) return KDA_ERR_ALIGN;
-  if (beta && !beta_aligned(beta, dtype)) return KDA_ERR_ALIGN;
-  if ((S0 && !aligned16(S0)) || (cu_seqlens && !aligned16(cu_seqlens))) return KDA_ERR_ALIGN;
-  int rc = check_common_opts(op);
+  int path = 0, snap_slots = 0;
+  int rc = kda::check_prefill(q, k, v, log_alpha, beta, S0, cu_seqlens, N, o, S_T, T_total, H,
+                              d_k, d_v, dtype, op, &path, &snap_slots);
   if (rc != KDA_OK) return rc;
-  // 64-bit extents: every index below 2^62
-  const long long tok_elems = (long long)T_total * H * d_k;
-  if (tok_elems < 0) return KDA_ERR_SHAPE;
-  // state snapshots every snapshot_every tokens (a multiple of the chunk)
-  int snap_slots = 0;
-  if (op->snapshot_every < 0 || (op->snapshot_every > 0 && op->snapshot_every % 64 != 0))
-    return KDA_ERR_ARG;
-  if (op->snapshot_every > 0) {
-    if (!op->snapshots) return KDA_ERR_ARG;
-    if (!aligned16(op->snapshots)) return KDA_ERR_ALIGN;
-    const int L = op->max_seqlen > 0 ? op->max_seqlen : (cu_seqlens ? T_total : T_total / N);
-    snap_slots = L / op->snapshot_every;
-  }
-
-  const int path = prefill_path(op, d_k, dtype);
-  if (path < 0) return KDA_ERR_UNSUPPORTED;
-  if (path == KDA_IMPL_SIMT && op->chunk == 64) return KDA_ERR_UNSUPPORTED;
 
   int* status = status_word();
   if (!status) return KDA_ERR_CUDA;

@@ -107,4 +107,18 @@ cudaError_t launch_gated_rmsnorm(const void* o, const void* gate, const float* w
 // Device address of the library's status word on the current device.
 int* status_word();
 
+// Unique id of the calling thread's current CUDA context, 0 if there is none
+// (or the driver cannot say).  Device addresses of the library's own device
+// variables are cached per (device, context id): a device reset creates a new
+// context, in which those variables live at new addresses.
+unsigned long long current_context_id();
+
+// Every host-side check of kda_prefill (everything but the workspace): returns
+// KDA_OK and the path (KDA_IMPL_SIMT or KDA_IMPL_TC) and the number of
+// snapshot slots per sequence, or the status code kda_prefill returns.
+int check_prefill(const void* q, const void* k, const void* v, const float* log_alpha,
+                  const void* beta, const float* S0, const int32_t* cu_seqlens, int N,
+                  const void* o, const float* S_T, int T_total, int H, int d_k, int d_v,
+                  int dtype, const kda_options* op, int* path_out, int* snap_slots_out);
+
 }  // namespace kda

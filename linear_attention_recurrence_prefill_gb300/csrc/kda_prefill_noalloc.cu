@@ -5,9 +5,12 @@
 // The scratch is a file-scope device array of KDA_NOALLOC_SCRATCH_BYTES
 // (64 MiB).  Every GPU that loads libkda.so holds it until the process exits.
 // In host code the array's name is only a host-side stand-in, never a device
-// address, so its device address is looked up once per device with
-// cudaGetSymbolAddress (with that device current) and handed to the kernels.
+// address, so its device address is looked up with cudaGetSymbolAddress, with
+// the device current, once per device (and again only if the device's context
+// was replaced, e.g. after a device reset), and handed to the kernels.
 #include <string.h>
+
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
@@ -18,19 +21,23 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {nullptr};
+unsigned long long g_scratch_ctx[kMaxDevices] = {0};
 
 // Device address of the scratch array on the current device (set up on the
-// first call per device).  Returns nullptr if the runtime refuses.
+// first call per device and context).  Returns nullptr if the runtime refuses.
 void* scratch_address() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-    g_scratch_addr[dev] = p;
-  }
-  return g_scratch_addr[dev];
+  const unsigned long long id = current_context_id();
+  std::lock_guard<std::mutex> g(g_scratch_mutex);
+  if (id != 0 && g_scratch_ctx[dev] == id && g_scratch_addr[dev]) return g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+  g_scratch_addr[dev] = p;
+  g_scratch_ctx[dev] = current_context_id();
+  return p;
 }
 
 }  // namespace
@@ -44,13 +51,21 @@ extern "C" int kda_prefill_noalloc(const void* q, const void* k, const void* v,
   kda_options op;
   if (opt) memcpy(&op, opt, sizeof(op));
   else kda_options_init(&op);
+  // only the tensor-core path (chunk 64) uses scratch; anything else is not
+  // offered here
   if (op.impl != KDA_IMPL_AUTO && op.impl != KDA_IMPL_TC) return KDA_ERR_UNSUPPORTED;
+  if (op.chunk != 0 && op.chunk != 64) return KDA_ERR_UNSUPPORTED;
   op.impl = KDA_IMPL_TC;
-  if (N < 1 || H < 1 || T_total < 0) return KDA_ERR_SHAPE;
-  if (dtype != KDA_BF16 || d_k != 128 || d_v != 128) return KDA_ERR_UNSUPPORTED;
+  // the same argument checks as kda_prefill, before anything is sized
+  int path = 0;
+  int rc = kda::check_prefill(q, k, v, log_alpha, beta, S0, cu_seqlens, N, o, S_T, T_total, H,
+                              d_k, d_v, dtype, &op, &path, nullptr);
+  if (rc != KDA_OK) return rc;
+  if (path != KDA_IMPL_TC) return KDA_ERR_UNSUPPORTED;
   // sizes whose scratch does not fit the built-in array are refused up front
-  const size_t need = kda_prefill_workspace_size(T_total, N, H, d_k, d_v, &op);
-  if (need == 0 || need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+  const size_t need = kda::tc_workspace_bytes(T_total, N, H, d_k, &op);
+  if (need == 0) return KDA_ERR_UNSUPPORTED;
+  if (need > (size_t)KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
   void* scratch = kda::scratch_address();
   if (!scratch) return KDA_ERR_CUDA;
   op.workspace = scratch;

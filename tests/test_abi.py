@@ -166,3 +166,35 @@ def test_workspace_size_is_zero_for_simt():
     assert kda.kda_prefill_workspace_size(4096, 1, 96, 128, 128,
                                           kda.kda_options_init(impl="simt")) == 0
     assert kda.kda_prefill_workspace_size(4096, 1, 96, 48, 48) == 0
+
+
+def _noalloc(**kw):
+    lib = kda.load()
+    args = dict(q=A, k=A, v=A, la=A, beta=A, S0=None, cu=None, N=1, o=A, S_T=A, T=64, H=2,
+                dk=128, dv=128, dtype=kda.KDA_BF16, opt=None)
+    args.update(kw)
+    opt = args["opt"] if args["opt"] is not None else kda.kda_options_init()
+    return lib.kda_prefill_noalloc(args["q"], args["k"], args["v"], args["la"], args["beta"],
+                                   args["S0"], args["cu"], args["N"], args["o"], args["S_T"],
+                                   args["T"], args["H"], args["dk"], args["dv"], args["dtype"],
+                                   ctypes.byref(opt), None)
+
+
+@no_gpu
+@pytest.mark.parametrize("kw,code", [
+    # what the tensor-core path does not take
+    (dict(opt=kda.kda_options_init(chunk=16)), kda.KDA_ERR_UNSUPPORTED),
+    (dict(opt=kda.kda_options_init(impl="simt")), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dtype=kda.KDA_F32), kda.KDA_ERR_UNSUPPORTED),
+    (dict(dk=64, dv=64), kda.KDA_ERR_UNSUPPORTED),
+    # kda_prefill's argument checks come before the scratch size, even for sizes
+    # far beyond the scratch
+    (dict(q=None, T=1 << 20, H=96), kda.KDA_ERR_ARG),
+    (dict(q=A + 8, T=1 << 20, H=96), kda.KDA_ERR_ALIGN),
+    (dict(dtype=7, T=1 << 20, H=96), kda.KDA_ERR_DTYPE),
+    (dict(opt=kda.kda_options_init(chunk=32)), kda.KDA_ERR_UNSUPPORTED),
+    # a valid call whose scratch exceeds the array
+    (dict(T=4096, H=96), kda.KDA_ERR_WORKSPACE),
+])
+def test_noalloc_rejects(kw, code):
+    assert _noalloc(**kw) == code

@@ -2,17 +2,20 @@
 memory (it uses a fixed scratch array built into the library instead of a
 caller-provided workspace).
 
-Called through the C ABI and checked against kda_prefill (the entry point with
-a caller-allocated workspace) on two calls in a row, within the bf16 tolerance
-the parity tests use.  The second call uses different inputs and sizes, so a
-result that leaned on the first call's leftovers in the shared scratch would
-show up.  This file is collected last on purpose.
+Called through the C ABI on two calls in a row and checked against kda_prefill
+(the entry point with a caller-allocated workspace): both run the same kernels
+with the same arithmetic, so the results must be equal bit for bit.  The second
+call uses different inputs and sizes, so a result that leaned on the first
+call's leftovers in the shared scratch would show up.  The first case is also
+compared with the CPU oracle, within the bf16 tolerance of the parity tests.
+This file is collected last on purpose.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 from linear_attention_recurrence_prefill_gb300 import inputs, kda
 from tests.parity_util import TOL_BF16, assert_close
 
@@ -44,15 +47,21 @@ def test_noalloc_matches_kda_prefill_twice():
     cases = [inputs.k3(dev, H=4, T=700, seed=31),
              inputs.varlen(dev, H=3, lengths=[130, 0, 257, 64])]
     cases[1].S0 = torch.randn((4, 3, 128, 128), device=dev) * 0.05
-    for inp in cases:
+    for i, inp in enumerate(cases):
         o = torch.empty_like(inp.q)
         S_T = torch.empty((inp.N, inp.H, 128, 128), dtype=torch.float32, device=dev)
         assert _noalloc_c(inp, o, S_T) == kda.KDA_OK
         torch.cuda.synchronize()
         assert kda.kda_get_last_error() == kda.KDA_OK
         o_ref, S_ref = _reference(inp)
-        assert_close(o, o_ref.float(), TOL_BF16, f"{inp.name} noalloc y")
-        assert_close(S_T, S_ref, TOL_BF16, f"{inp.name} noalloc S_T")
+        assert torch.equal(o, o_ref), f"{inp.name}: noalloc y differs from kda_prefill"
+        assert torch.equal(S_T, S_ref), f"{inp.name}: noalloc S_T differs from kda_prefill"
+        if i == 0:
+            o_orc, S_orc = oracle.prefill(inp.q.cpu(), inp.k.cpu(), inp.v.cpu(),
+                                          inp.log_alpha.cpu(), inp.beta.cpu(), inp.S0.cpu())
+            y_orc = oracle.gated_rmsnorm(o_orc, inp.gate.cpu())
+            assert_close(o, y_orc, TOL_BF16, f"{inp.name} noalloc y vs oracle")
+            assert_close(S_T, S_orc, TOL_BF16, f"{inp.name} noalloc S_T vs oracle")
 
 
 def test_noalloc_refuses_sizes_beyond_the_scratch():
