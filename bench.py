@@ -6,9 +6,13 @@ gate, fp32 log alpha and states, gated RMSNorm output): every prefill row of
 the hot path (prologue, decay rescale, Gram, UT solve, W/U, state chain,
 output, epilogue).  ``value`` is prefill tokens/s over all ranks with inputs
 resident in HBM; the one-token decode step (64 sequences x 96 heads, state in
-place) is measured in the same run and reported under ``decode``.
+place) is measured in the same run and reported under ``decode``, and so are
+the varlen prefill (8 packed sequences of 1,024..16,384 tokens) and the
+decay-extreme prefill (T = 262,144), under ``prefill_varlen`` and
+``prefill_extreme``.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--legs prefill,e2e,decode,varlen,extreme]
 
 Multi-GPU runs are independent replicas (the path has no exchange step): each
 rank runs the same workload, ``value`` = total tokens / max-over-ranks time.
@@ -18,8 +22,11 @@ workload on the host cores (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -44,8 +51,10 @@ WS_BLOCK_BYTES = 74240  # tensor-core path: workspace block per (64-token chunk,
 DEC_BYTES_PER_UNIT = 2 * STATE_BYTES + 4 * 2 * D + 4 * D + 2
 
 
-def prefill_bytes(T_=T, H_=H, N_=1):
-    return BYTES_PER_TOKEN_HEAD * T_ * H_ + 2 * STATE_BYTES * H_ * N_
+def prefill_bytes(T_=T, H_=H, N_=1, s0=True):
+    """Method bytes of one call: 1,794 B per (token, head), and per (sequence,
+    head) the state written once, and read once when an initial state is given."""
+    return BYTES_PER_TOKEN_HEAD * T_ * H_ + (2 if s0 else 1) * STATE_BYTES * H_ * N_
 
 
 def prefill_flops(chunk: int, T_=T, H_=H, d=D):
@@ -54,39 +63,65 @@ def prefill_flops(chunk: int, T_=T, H_=H, d=D):
     return (6 * d * d + 4 * chunk * d + chunk * chunk / 3.0) * T_ * H_
 
 
-# DRAM bytes (read + write) per launch from an ncu capture of the kernel as it
-# stands (profiles/ holds the summaries); None until captured after a change.
-TRAFFIC: dict[str, float | None] = {
-    # profiles/prep_kernel_k3_prefill.md, profiles/chain_kernel_k3_prefill.md
-    # (dram read + write of one launch)
-    "prep_kernel": 504.551424e6 + 407.481856e6,
-    "chain_kernel": 563.14752e6 + 87.442688e6,
-    # profiles/decode_kernel_k3_decode.md
-    "decode_kernel<128,bf16>": 410.566656e6 + 343.659776e6,
-}
+def code_sha16(path: str) -> str:
+    """Hash of a source file's code: comments and whitespace stripped, so that
+    an edit of a comment does not count as a change of the kernel."""
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    src = re.sub(r"\s+", "", src)
+    return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
-def kernel_plan(path: str, chunk: int):
-    """(kernel, roofline bound, algorithmic bytes, algorithmic flops) per launch
-    of one prefill call, in launch order."""
+def measured_traffic() -> dict:
+    """DRAM bytes (read + write) per launch of each kernel, from the ncu
+    summaries under profiles/: lines of the form
+
+        traffic: kernel=<name> bytes_per_launch=<B> source=<file> code_sha16=<h>
+
+    An entry counts only while the kernel's source file still has the code it
+    had when the counters were taken (same code_sha16); otherwise the kernel
+    has changed since, and its traffic is unknown (None)."""
+    out = {}
+    for fn in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(fn) as f:
+            for line in f:
+                if not line.startswith("traffic:"):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
+                src = os.path.join(ROOT, kv.get("source", ""))
+                if os.path.isfile(src) and code_sha16(src) == kv.get("code_sha16"):
+                    out[kv["kernel"]] = float(kv["bytes_per_launch"])
+    return out
+
+
+def kernel_plan(path: str, chunk: int, T_=T, H_=H, N_=1, chunks=None):
+    """(kernel, roofline bound, method bytes, algorithmic flops, workspace bytes)
+    per launch of one prefill call, in launch order.  Method bytes are the
+    method's own inputs and outputs that the kernel reads or writes (the
+    1,794 B per token and head of the call, and the states); the workspace the
+    tensor-core path passes from its second kernel to its third is counted
+    apart."""
     if path == "simt":
-        return [("prefill_simt_kernel<128,bf16>", "hbm", prefill_bytes(), prefill_flops(16))]
+        return [("prefill_simt_kernel<128,bf16>", "hbm", prefill_bytes(T_, H_, N_),
+                 prefill_flops(16, T_, H_), 0)]
     if path == "tc":
-        chunks = (T // chunk) * H
-        ws = WS_BLOCK_BYTES * chunks
-        # prep: reads q, k, v, log alpha, beta; writes one operand block per (chunk, head)
-        prep_b = (3 * 2 * D + 4 * D + 2) * T * H + ws
-        # chain: reads the blocks and the gate, writes y, reads S0 and writes S_T
-        chain_b = ws + 2 * 2 * D * T * H + 2 * STATE_BYTES * H
+        nck = chunks if chunks is not None else (T_ // chunk) * H_
+        ws = WS_BLOCK_BYTES * nck
+        # prep reads q, k, v, log alpha and beta; chain reads the gate, writes y
+        # and reads S0 / writes S_T
+        prep_b = (3 * 2 * D + 4 * D + 2) * T_ * H_
+        chain_b = 2 * 2 * D * T_ * H_ + 2 * STATE_BYTES * H_ * N_
         # tensor-core flops issued per (chunk, head): Gram 3 x 4 x (128x16x128);
         # U~ 2 x (128x64x64) (T as a bf16 hi/lo pair); W 128x128x64.  Chain:
         # [D | O] 128x128x128, S += U K^ 128x128x64, O += U P^T 128x64x64
         prep_f = (3 * 4 * 2 * 128 * 16 * 128 + 2 * 2 * 128 * 64 * 64
-                  + 2 * 128 * 128 * 64) * chunks
-        chain_f = (2 * 128 * 128 * 128 + 2 * 128 * 128 * 64 + 2 * 128 * 64 * 64) * chunks
-        return [("chunk_base_kernel", "hbm", 4 * 2, 0.0),
-                ("prep_kernel", "hbm", prep_b, prep_f),
-                ("chain_kernel", "hbm", chain_b, chain_f)]
+                  + 2 * 128 * 128 * 64) * nck
+        chain_f = (2 * 128 * 128 * 128 + 2 * 128 * 128 * 64 + 2 * 128 * 64 * 64) * nck
+        return [("chunk_base_kernel", "hbm", 4 * 2 * N_, 0.0, 0),
+                ("prep_kernel", "hbm", prep_b, prep_f, ws),
+                ("chain_kernel", "hbm", chain_b, chain_f, ws)]
     raise ValueError(f"no kernel plan for path {path}")
 
 
@@ -197,6 +232,90 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ our arm
 N_UP = 4  # host->device copy streams of the end-to-end leg
+LEGS = ("prefill", "e2e", "decode", "varlen", "extreme")
+
+
+def time_prefill(inp, args, stream, dist, *, steps, warmup, max_seqlen=0, clocks=False):
+    """Device time of one kda_prefill call on `inp` (inputs resident in HBM):
+    `warmup` untimed calls, then `steps` calls between CUDA events on the
+    launching stream, a barrier and a synchronise on both sides; then the
+    per-kernel times from events the library records around each of its
+    kernels, over a second pass of the same calls."""
+    import torch
+
+    from linear_attention_recurrence_prefill_gb300 import kda
+
+    dev = inp.q.device
+    N = inp.N
+    o = torch.empty_like(inp.q)
+    S_T = torch.empty((N, inp.H, D, D), dtype=torch.float32, device=dev)
+    o_opts = kda.kda_options_init(impl=kda.IMPLS[args.path], max_seqlen=max_seqlen)
+    ws_bytes = kda.kda_prefill_workspace_size(inp.T, N, inp.H, D, D, o_opts)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    path, launches, chunk = kda.kda_prefill_path(inp.T, N, inp.H, D, D, kda.KDA_BF16, o_opts)
+
+    def call(events=None):
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0, inp.cu_seqlens, N,
+                        o, S_T, gate=inp.gate, impl=args.path, max_seqlen=max_seqlen,
+                        workspace=ws if ws_bytes else None, phase_events=events)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    if kda.kda_get_last_error() != kda.KDA_OK:
+        raise RuntimeError(f"device status word set during the {inp.name} warm-up")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(torch.cuda.current_device()) if clocks else None
+    if clk:
+        clk.__enter__()
+    try:
+        barrier(dist)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(steps):
+            call()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    finally:
+        if clk:
+            clk.__exit__(None, None, None)
+    ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / steps)
+    per = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)]
+           for _ in range(steps)]
+    for evs in per:        # torch creates the CUDA event on first record
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for evs in per:
+        call(evs)
+    torch.cuda.synchronize()
+    if kda.kda_get_last_error() != kda.KDA_OK:
+        raise RuntimeError(f"device status word set during the {inp.name} calls")
+    kern = []
+    for i in range(launches):
+        kern.append(statistics.mean(evs[i].elapsed_time(evs[i + 1]) for evs in per))
+    del ws, o, S_T
+    return dict(ms=ms, path=path, chunk=chunk, launches=launches, kernel_ms=kern,
+                ws_bytes=ws_bytes, clocks=clk.summary() if clk else None)
+
+
+def prefill_leg(inp, args, stream, dist, peaks, *, steps, warmup, max_seqlen=0):
+    """Tokens/s and the HBM fraction on the method's bytes for one workload."""
+    lens = inp.meta.get("lengths") or [inp.T // inp.N] * inp.N
+    r = time_prefill(inp, args, stream, dist, steps=steps, warmup=warmup, max_seqlen=max_seqlen)
+    tokens = inp.T
+    nbytes = prefill_bytes(tokens, inp.H, inp.N, s0=inp.S0 is not None)
+    chunks = sum((L + r["chunk"] - 1) // r["chunk"] for L in lens) * inp.H \
+        if r["path"] == "tc" else None
+    plan = kernel_plan(r["path"], r["chunk"], tokens, inp.H, inp.N, chunks)
+    return {"workload": inp.name, "tokens": tokens, "sequences": inp.N, "steps": steps,
+            "warmup": warmup, "ms_per_step": r["ms"],
+            "value": tokens * int(os.environ.get("WORLD_SIZE", "1")) / (r["ms"] / 1e3),
+            "unit": "tokens/s", "method_bytes": nbytes,
+            "hbm_frac": nbytes / (r["ms"] / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "kernel_ms": {plan[i][0]: r["kernel_ms"][i] for i in range(r["launches"])},
+            "path": r["path"], "chunk": r["chunk"]}
 
 
 def run_ours(args, rank, world, local, dist):
@@ -207,69 +326,101 @@ def run_ours(args, rank, world, local, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     peaks = load_peaks()
+    traffic = measured_traffic()
     kda.load()
+    legs = set(args.legs.split(","))
+    stream = torch.cuda.current_stream()
+    line = {}
 
+    # --- the K3-shaped prefill: the headline number (inputs resident; 688 MB
+    # of token inputs per step, larger than L2) ---
     inp = inputs.k3(dev)
-    opt = dict(gate=inp.gate, impl=args.path)
-    # outputs and workspace allocated once, outside the timed region
-    o = torch.empty_like(inp.q)
-    S_T = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
-    o_opts = kda.kda_options_init(impl=kda.IMPLS[args.path])
-    ws_bytes = kda.kda_prefill_workspace_size(T, 1, H, D, D, o_opts)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    path, launches, chunk = kda.kda_prefill_path(T, 1, H, D, D, kda.KDA_BF16, o_opts)
+    r = time_prefill(inp, args, stream, dist, steps=args.steps, warmup=args.warmup, clocks=True)
+    ms_max, path, chunk, launches = r["ms"], r["path"], r["chunk"], r["launches"]
     kernels = kernel_plan(path, chunk)
     assert len(kernels) == launches, (kernels, launches)
-    stream = torch.cuda.current_stream()
+    kern_ms = {kernels[i][0]: r["kernel_ms"][i] for i in range(launches)}
+    dom_i = max(range(launches), key=lambda i: r["kernel_ms"][i])
+    dom, dom_bound, dom_method_bytes, dom_flops, dom_ws = kernels[dom_i]
+    dom_ms = r["kernel_ms"][dom_i]
+    call_bytes = prefill_bytes()
+    # the roofline of the dominant kernel on the method's bytes of the whole
+    # call: every kernel of the call exists to move those bytes, so this is
+    # the fraction of HBM the call would reach if it took the dominant
+    # kernel's time
+    achieved = call_bytes / (dom_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic.get(dom), "kernel": dom,
+            "kernel_ms": dom_ms, "algorithmic_bytes": call_bytes,
+            "kernel_method_bytes": dom_method_bytes,
+            "kernel_method_frac": dom_method_bytes / (dom_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "workspace_bytes": dom_ws,
+            "workspace_note": "operand blocks the tensor-core path writes in its second kernel "
+                              "and reads in its third (not method bytes)",
+            "tensor_tflops": dom_flops / (dom_ms / 1e3) / 1e12,
+            "tensor_frac": dom_flops / (dom_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+            "peak_src": "of measured (MEASURED_PEAKS.json, burst)"
+            if peaks["src"] == "measured" else "of fallback"}
+    tokens = T * world
+    line.update({
+        "metric": METRIC, "value": tokens / (ms_max / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T, "heads": H,
+                   "head_dim": D, "parallelism": f"replicas x{world}" if world > 1 else "single",
+                   "path": path, "chunk": chunk,
+                   "l2": "inputs larger than L2 (688 MB of token inputs per step)"},
+        "prefill": {"hbm_gbs_algorithmic": call_bytes / (ms_max / 1e3) / 1e9,
+                    "hbm_frac": call_bytes / (ms_max / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    "tflops_algorithmic": prefill_flops(chunk) / (ms_max / 1e3) / 1e12,
+                    "kernel_ms": kern_ms,
+                    "traffic_per_launch": {k[0]: traffic.get(k[0]) for k in kernels}},
+        "roofline": roof,
+        "clocks": r["clocks"],
+        "gpu_launches": launches * args.steps,
+    })
 
-    def step(events=None):
-        kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0, None, 1, o, S_T,
-                        workspace=ws if ws_bytes else None, phase_events=events, **opt)
+    if "e2e" in legs:
+        line["e2e"] = run_e2e(args, inp, stream, dist, tokens, world)
+    del inp
+    torch.cuda.empty_cache()
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    if kda.kda_get_last_error() != kda.KDA_OK:
-        raise RuntimeError("device status word set during warm-up")
+    if "decode" in legs:
+        line["decode"] = run_decode(args, dev, stream, dist, peaks, traffic)
+        torch.cuda.empty_cache()
+    for name in ("varlen", "extreme"):
+        if name not in legs:
+            continue
+        w = inputs.varlen(dev) if name == "varlen" else inputs.extreme(dev)
+        ms_len = max(w.meta["lengths"]) if name == "varlen" else 0
+        line[f"prefill_{name}"] = prefill_leg(w, args, stream, dist, peaks,
+                                              steps=max(3, min(args.steps, 10)), warmup=3,
+                                              max_seqlen=ms_len)
+        del w
+        torch.cuda.empty_cache()
 
-    # --- device-timed region (inputs resident; 688 MB of inputs > L2) ---
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(dist)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms_max = max_over_ranks(dist, ms)
-    clocks = clk.summary()
+    # --- CPU baseline (oracle) on rank 0 at N=1 ---
+    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    line["cpu_baseline"] = cpu
+    return line if rank == 0 else None
 
-    # --- per-kernel durations: events the library records around each of its
-    # kernels on the launching stream, over a second pass of the same steps ---
-    per = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)]
-           for _ in range(args.steps)]
-    for evs in per:        # torch creates the CUDA event on first record
-        for e in evs:
-            e.record(stream)
-    torch.cuda.synchronize()
-    for evs in per:
-        step(evs)
-    torch.cuda.synchronize()
-    kern_ms = {}
-    for i, (name, *_rest) in enumerate(kernels):
-        kern_ms[name] = statistics.mean(evs[i].elapsed_time(evs[i + 1]) for evs in per)
-    dom_i = max(range(launches), key=lambda i: kern_ms[kernels[i][0]])
-    dom, dom_bound, dom_bytes, dom_flops = kernels[dom_i]
-    dom_ms = kern_ms[dom]
 
-    # --- end to end through the public API with host buffers ---
-    # A serving loop pipelines steps: step i+1's inputs go up (two copy
-    # streams, double-buffered device inputs and outputs) while step i runs,
-    # and step i's results come back on a third stream.  Every step's own
-    # host->device and device->host copies are inside the timed region.
+def run_e2e(args, inp, stream, dist, tokens, world):
+    """The same metric end to end through the public API, host buffers in and
+    out.  A serving loop pipelines steps: step i+1's inputs go up (several copy
+    streams, double-buffered device inputs and outputs) while step i runs, and
+    step i's results come back on another stream.  Every step's own
+    host->device and device->host copies are inside the timed region."""
+    import torch
+
+    from linear_attention_recurrence_prefill_gb300 import kda
+
+    o = torch.empty_like(inp.q)
+    S_T = torch.empty((1, H, D, D), dtype=torch.float32, device=inp.q.device)
+    o_opts = kda.kda_options_init(impl=kda.IMPLS[args.path])
+    ws_bytes = kda.kda_prefill_workspace_size(T, 1, H, D, D, o_opts)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=inp.q.device)
     host = {n: getattr(inp, n).cpu().pin_memory() for n in
             ("q", "k", "v", "log_alpha", "beta", "gate", "S0")}
     devb = [{n: torch.empty_like(getattr(inp, n)) for n in host} for _ in range(2)]
@@ -329,6 +480,7 @@ def run_ours(args, rank, world, local, dist):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier(dist)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for st in up + [down]:
         st.wait_stream(stream)
@@ -338,55 +490,12 @@ def run_ours(args, rank, world, local, dist):
     ev1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / e2e_steps)
-    del host, devb, outs
-
-    # --- decode (state in place; 805 MB of state > L2) ---
-    dec = run_decode(args, dev, stream, dist, peaks)
-
-    # --- CPU baseline (oracle) on rank 0 at N=1 ---
-    cpu = cpu_baseline(args) if (rank == 0 and world == 1 and not args.no_cpu) else None
-
-    if rank != 0:
-        return None
-    tokens = T * world
-    value = tokens / (ms_max / 1e3)
-    if dom_bound == "tensor":
-        achieved = dom_flops / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"]}
-    else:
-        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    roof.update({"traffic": TRAFFIC.get(dom), "kernel": dom, "kernel_ms": dom_ms,
-                 "algorithmic_bytes": dom_bytes, "algorithmic_flops": dom_flops,
-                 "peak_src": "of measured (MEASURED_PEAKS.json, burst)"
-                 if peaks["src"] == "measured" else "of fallback"})
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T, "heads": H,
-                   "head_dim": D, "parallelism": f"replicas x{world}" if world > 1 else "single",
-                   "path": path, "chunk": chunk,
-                   "l2": "inputs larger than L2 (688 MB of token inputs per step)"},
-        "prefill": {"hbm_gbs_algorithmic": prefill_bytes() / (ms_max / 1e3) / 1e9,
-                    "hbm_frac": prefill_bytes() / (ms_max / 1e3) / 1e9 / peaks["hbm_gbs"],
-                    "tflops_algorithmic": prefill_flops(chunk) / (ms_max / 1e3) / 1e12,
-                    "kernel_ms": kern_ms},
-        "roofline": roof,
-        "decode": dec,
-        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "cpu_baseline": cpu,
-        "clocks": clocks,
-        "gpu_launches": launches * args.steps,
-    }
-    return line
+    del host, devb, outs, ws
+    return {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
-def run_decode(args, dev, stream, dist, peaks):
+def run_decode(args, dev, stream, dist, peaks, traffic):
     import torch
 
     from linear_attention_recurrence_prefill_gb300 import inputs, kda
@@ -437,7 +546,7 @@ def run_decode(args, dev, stream, dist, peaks):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": bytes_step,
                          "kernel": "decode_kernel<128,bf16>",
-                         "traffic": TRAFFIC.get("decode_kernel<128,bf16>")},
+                         "traffic": traffic.get("decode_kernel<128,bf16>")},
             "gpu_launches": DEC_STEPS * reps}
 
 
@@ -526,7 +635,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of CPU work for the oracle sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU baseline leg")
+    ap.add_argument("--legs", default=",".join(LEGS),
+                    help="comma list of what to measure besides the K3-shaped prefill: "
+                         + ", ".join(LEGS[1:]) + " (default: all)")
     args = ap.parse_args(argv)
+    bad = set(args.legs.split(",")) - set(LEGS)
+    if bad:
+        ap.error(f"unknown legs: {sorted(bad)}")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

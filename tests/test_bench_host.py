@@ -74,3 +74,29 @@ def test_reference_arm_line(capsys):
 def test_warmup_floor():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_code_hash_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("// head\n__global__ void k(int* x) { x[0] = 1; /* one */ }\n")
+    h = bench.code_sha16(str(a))
+    a.write_text("// another head\n__global__ void k(int* x) {\n  x[0] = 1;  // one\n}\n")
+    assert bench.code_sha16(str(a)) == h
+    a.write_text("__global__ void k(int* x) { x[0] = 2; }\n")
+    assert bench.code_sha16(str(a)) != h
+
+
+def test_measured_traffic_follows_the_code(tmp_path, monkeypatch):
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void k() {}\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    h = bench.code_sha16(str(src))
+    (prof / "k.md").write_text(
+        "notes\n"
+        f"traffic: kernel=k bytes_per_launch=1234 source=k.cu code_sha16={h}\n"
+        "traffic: kernel=old bytes_per_launch=99 source=k.cu code_sha16=0000000000000000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic() == {"k": 1234.0}
+    src.write_text("__global__ void k() { int a = 0; }\n")   # the kernel changed
+    assert bench.measured_traffic() == {}
