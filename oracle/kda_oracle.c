@@ -9,6 +9,14 @@
  *
  * What it computes, per sequence, per head, per token t (the pages' order):
  *
+ *   0. (optional) each of q, k, v passes through a causal depthwise
+ *      convolution of width 4 over the tokens of its sequence, then Swish,
+ *      x * sigmoid(x) ("Kimi K3's hybrid block, from first principles",
+ *      section "From linear attention to the delta rule": queries and keys go
+ *      through a short convolution of width 4, Swish and L2 normalisation,
+ *      values through the convolution and Swish).  Taps w[c][0..3] weigh the
+ *      raw rows t-3 .. t, oldest first; rows before the sequence start are
+ *      the caller's window of earlier rows, zeros by default.
  *   1. q <- q / sqrt(sum q^2 + eps), k likewise (optional; the layer applies
  *      L2 normalisation to queries and keys: "Kimi K3's hybrid block, from
  *      first principles", section "From linear attention to the delta rule").
@@ -17,7 +25,14 @@
  *   3. a = exp(clamp(log alpha, g_min, 0)), g_min = -5: the retention factor of
  *      every key channel lies in [e^-5, 1] ("Kimi K3", section "Forgetting
  *      different features at different rates"; the hybrid-block page, same
- *      section as above, on the bounded log-decay).
+ *      section as above, on the bounded log-decay).  Optionally log alpha is
+ *      formed from the decay logit z (a low-rank projection plus a per-channel
+ *      bias b) with one scale A_h per head, through a bounded sigmoid:
+ *      log alpha = g_min * sigmoid(A_h (z + b)) (same section: the log-decay is
+ *      bounded from below with a learned per-head scale; "What changed": the
+ *      mapping went from an unbounded softplus to a bounded sigmoid; the
+ *      printed formula itself did not survive, this is the plainest form that
+ *      keeps every factor in [e^g_min, 1]).
  *   4. S <- Diag(a) S                 (fade first)
  *   5. u = S^T k                      (what the memory now predicts for k)
  *   6. S <- S + beta k (v - u)^T      (erase the old association, write v)
@@ -59,7 +74,18 @@ typedef struct {
   double g_min;      /* floor of log alpha (the pages' value is -5)          */
   double q_scale;    /* multiplier on the read-out (1 by default)            */
   double eps_l2;     /* epsilon inside the L2-norm square root                */
+  int decay_from_logit;      /* 1: log_alpha holds decay logits z; log alpha =
+                                g_min * sigmoid(A_h (z + b_{h,c}))            */
+  const double* decay_scale; /* A [H], NULL = ones                            */
+  const double* decay_bias;  /* b [H][dk], NULL = zeros                       */
+  const double* conv_weight; /* NULL: no short convolution.  Else taps
+                                [3 (q, k, v)][H][d][4], oldest row first
+                                (needs dk == dv == d)                        */
 } kda_oracle_opts;
+
+/* Raw rows of q, k, v before the current token, per tensor the 3 previous
+ * rows oldest first: hist[(X * 3 + j) * d + c]. */
+enum { CONV_W = 4, CONV_HIST = CONV_W - 1 };
 
 enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F64 = 2 };
 
@@ -183,12 +209,43 @@ static void token_step(double* S, int dk, int dv, const double* q,
 #endif
 }
 
-/* Steps 1-2 for one (token, head): widen, normalise and activate. */
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Step 0 for one tensor X (0 = q, 1 = k, 2 = v) of one (token, head h of H):
+ * x holds the raw row and receives conv + Swish; the raw row enters the
+ * history. */
+static void conv_swish(double* x, int X, int H, int h, int d, const kda_oracle_opts* opt,
+                       double* hist) {
+  double* hx = hist + (size_t)X * CONV_HIST * d;
+  for (int c = 0; c < d; ++c) {
+    const double* wc = opt->conv_weight + (((size_t)X * H + h) * d + c) * CONV_W;
+    double y = 0.0;
+#if KDA_ORACLE_MUTATION == 12
+    /* planted mistake: taps applied newest row first */
+    for (int j = 0; j < CONV_HIST; ++j) y += wc[CONV_W - 1 - j] * hx[(size_t)j * d + c];
+    y += wc[0] * x[c];
+#else
+    for (int j = 0; j < CONV_HIST; ++j) y += wc[j] * hx[(size_t)j * d + c];
+    y += wc[CONV_W - 1] * x[c];
+#endif
+    for (int j = 0; j + 1 < CONV_HIST; ++j) hx[(size_t)j * d + c] = hx[(size_t)(j + 1) * d + c];
+    hx[(size_t)(CONV_HIST - 1) * d + c] = x[c];
+#if KDA_ORACLE_MUTATION == 13
+    x[c] = (X == 2) ? y : y * sigmoid(y); /* planted mistake: no Swish on v */
+#else
+    x[c] = y * sigmoid(y);
+#endif
+  }
+}
+
+/* Steps 0-3 for one (token, head): widen, convolve (optional), normalise and
+ * activate.  hist: the raw-row history of this (sequence, head), used and
+ * advanced when the convolution is on. */
 static void prologue(const void* q, const void* k, const void* v, int qkv_dtype,
                      const void* log_alpha, int la_dtype, const void* beta,
                      int beta_dtype, size_t row, int H, int h, int dk, int dv,
-                     const kda_oracle_opts* opt, double* qd, double* kd,
-                     double* vd, double* lad, double* bd) {
+                     const kda_oracle_opts* opt, double* hist, double* qd,
+                     double* kd, double* vd, double* lad, double* bd) {
   const size_t qk_off = (row * (size_t)H + (size_t)h) * (size_t)dk;
   const size_t v_off = (row * (size_t)H + (size_t)h) * (size_t)dv;
   for (int c = 0; c < dk; ++c) {
@@ -197,8 +254,26 @@ static void prologue(const void* q, const void* k, const void* v, int qkv_dtype,
     lad[c] = load_elem(log_alpha, la_dtype, qk_off + c);
   }
   for (int j = 0; j < dv; ++j) vd[j] = load_elem(v, qkv_dtype, v_off + j);
+  if (opt->conv_weight) {
+    conv_swish(qd, 0, H, h, dk, opt, hist);
+    conv_swish(kd, 1, H, h, dk, opt, hist);
+    conv_swish(vd, 2, H, h, dv, opt, hist);
+  }
+  if (opt->decay_from_logit) {
+    const double A = opt->decay_scale ? opt->decay_scale[h] : 1.0;
+    for (int c = 0; c < dk; ++c) {
+      const double z = lad[c] + (opt->decay_bias ? opt->decay_bias[(size_t)h * dk + c] : 0.0);
+#if KDA_ORACLE_MUTATION == 14
+      lad[c] = -log1p(exp(A * z)); /* planted mistake: the old unbounded softplus */
+#elif KDA_ORACLE_MUTATION == 15
+      lad[c] = A * opt->g_min * sigmoid(z); /* planted mistake: scale outside */
+#else
+      lad[c] = opt->g_min * sigmoid(A * z);
+#endif
+    }
+  }
   double b = load_elem(beta, beta_dtype, row * (size_t)H + (size_t)h);
-  if (opt->beta_is_logit) b = 1.0 / (1.0 + exp(-b));
+  if (opt->beta_is_logit) b = sigmoid(b);
   *bd = b;
   if (opt->l2norm_qk) {
     l2_normalise(qd, dk, opt->eps_l2);
@@ -206,6 +281,32 @@ static void prologue(const void* q, const void* k, const void* v, int qkv_dtype,
     l2_normalise(kd, dk, opt->eps_l2);
 #endif
   }
+}
+
+/* History of one (sequence n, head h) from the caller's window
+ * conv_state [N][3][3][H][d] (fp64, NULL = zeros). */
+static void init_hist(double* hist, const double* conv_state, int n, int H, int h, int d) {
+  for (int X = 0; X < 3; ++X)
+    for (int j = 0; j < CONV_HIST; ++j)
+      for (int c = 0; c < d; ++c) {
+#if KDA_ORACLE_MUTATION == 16
+        const int jj = CONV_HIST - 1 - j; /* planted mistake: window read newest first */
+#else
+        const int jj = j;
+#endif
+        hist[((size_t)X * CONV_HIST + j) * d + c] =
+            conv_state ? conv_state[((((size_t)n * 3 + X) * CONV_HIST + jj) * H + h) * d + c]
+                       : 0.0;
+      }
+}
+
+/* Back into the caller's window. */
+static void store_hist(const double* hist, double* conv_state, int n, int H, int h, int d) {
+  for (int X = 0; X < 3; ++X)
+    for (int j = 0; j < CONV_HIST; ++j)
+      for (int c = 0; c < d; ++c)
+        conv_state[((((size_t)n * 3 + X) * CONV_HIST + j) * H + h) * d + c] =
+            hist[((size_t)X * CONV_HIST + j) * d + c];
 }
 
 /*
@@ -220,6 +321,9 @@ static void prologue(const void* q, const void* k, const void* v, int qkv_dtype,
  *   heads h0 .. h0+nh-1 are computed (a subset keeps full-size checks cheap)
  *   o           [T_total][nh][dv] fp64 out
  *   S_T         [N][nh][dk][dv]   fp64 out (NULL = not wanted)
+ *   conv_state  [N][3][3][H][d] fp64, NULL = zeros: with opt->conv_weight, the
+ *               raw q, k, v rows of the 3 tokens before each sequence, oldest
+ *               first (read only)
  *
  * Returns 0, or -1 on a bad argument.
  */
@@ -228,9 +332,11 @@ int kda_oracle_prefill(const void* q, const void* k, const void* v, int qkv_dtyp
                        int beta_dtype, const double* S0,
                        const int32_t* cu_seqlens, int N, int T_total, int H,
                        int dk, int dv, int h0, int nh,
-                       const kda_oracle_opts* opt, double* o, double* S_T) {
+                       const kda_oracle_opts* opt, double* o, double* S_T,
+                       const double* conv_state) {
   if (!q || !k || !v || !log_alpha || !beta || !o || !opt) return -1;
   if (N < 1 || T_total < 0 || H < 1 || dk < 1 || dv < 1) return -1;
+  if (opt->conv_weight && dk != dv) return -1;
   if (h0 < 0 || nh < 1 || h0 + nh > H) return -1;
   if (!dtype_ok(qkv_dtype) || !dtype_ok(la_dtype) || !dtype_ok(beta_dtype)) return -1;
   if (!cu_seqlens && (T_total % N) != 0) return -1;
@@ -247,7 +353,7 @@ int kda_oracle_prefill(const void* q, const void* k, const void* v, int qkv_dtyp
     const int t0 = cu_seqlens ? cu_seqlens[n] : n * (T_total / N);
     const int t1 = cu_seqlens ? cu_seqlens[n + 1] : (n + 1) * (T_total / N);
     double* S = (double*)malloc(sizeof(double) * (size_t)dk * dv);
-    double* buf = (double*)malloc(sizeof(double) * (size_t)(3 * dk + 3 * dv));
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(3 * dk + 3 * dv + 9 * dk));
     if (!S || !buf) {
       free(S);
       free(buf);
@@ -256,14 +362,27 @@ int kda_oracle_prefill(const void* q, const void* k, const void* v, int qkv_dtyp
       continue;
     }
     double *qd = buf, *kd = buf + dk, *lad = buf + 2 * dk;
-    double *vd = buf + 3 * dk, *u = vd + dv, *ot = u + dv;
+    double *vd = buf + 3 * dk, *u = vd + dv, *ot = u + dv, *hist = ot + dv;
     const size_t SS = (size_t)dk * dv;
     if (S0) memcpy(S, S0 + ((size_t)n * H + h) * SS, sizeof(double) * SS);
     else memset(S, 0, sizeof(double) * SS);
+    if (opt->conv_weight) init_hist(hist, conv_state, n, H, h, dk);
+#if KDA_ORACLE_MUTATION == 17
+    /* planted mistake: the window is the packed rows before the sequence,
+       whichever sequence they belong to */
+    if (opt->conv_weight && t0 >= CONV_HIST)
+      for (int j = 0; j < CONV_HIST; ++j)
+        for (int c = 0; c < dk; ++c) {
+          const size_t off = ((size_t)(t0 - CONV_HIST + j) * H + h) * dk + c;
+          hist[(0 * CONV_HIST + j) * (size_t)dk + c] = load_elem(q, qkv_dtype, off);
+          hist[(1 * CONV_HIST + j) * (size_t)dk + c] = load_elem(k, qkv_dtype, off);
+          hist[(2 * CONV_HIST + j) * (size_t)dk + c] = load_elem(v, qkv_dtype, off);
+        }
+#endif
     for (int t = t0; t < t1; ++t) {
       double b;
       prologue(q, k, v, qkv_dtype, log_alpha, la_dtype, beta, beta_dtype,
-               (size_t)t, H, h, dk, dv, opt, qd, kd, vd, lad, &b);
+               (size_t)t, H, h, dk, dv, opt, hist, qd, kd, vd, lad, &b);
       token_step(S, dk, dv, qd, kd, vd, lad, b, opt, u, ot);
       memcpy(o + ((size_t)t * nh + hh) * dv, ot, sizeof(double) * dv);
     }
@@ -278,32 +397,37 @@ int kda_oracle_prefill(const void* q, const void* k, const void* v, int qkv_dtyp
  * One recurrent decode step for N independent sequences, state updated in
  * place: the same token recurrence as above, applied once.
  *   q, k [N][H][dk]; v [N][H][dv]; log_alpha [N][H][dk]; beta [N][H];
- *   S [N][H][dk][dv] fp64 in/out; o [N][H][dv] fp64 out.
+ *   S [N][H][dk][dv] fp64 in/out; o [N][H][dv] fp64 out;
+ *   conv_state [N][3][3][H][d] fp64 in/out with opt->conv_weight (the raw
+ *   rows of the 3 previous tokens, oldest first; NULL = zeros, not kept).
  */
 int kda_oracle_decode_step(const void* q, const void* k, const void* v,
                            int qkv_dtype, const void* log_alpha, int la_dtype,
                            const void* beta, int beta_dtype, double* S, int N,
                            int H, int dk, int dv, const kda_oracle_opts* opt,
-                           double* o) {
+                           double* o, double* conv_state) {
   if (!q || !k || !v || !log_alpha || !beta || !S || !o || !opt) return -1;
   if (N < 1 || H < 1 || dk < 1 || dv < 1) return -1;
+  if (opt->conv_weight && dk != dv) return -1;
   if (!dtype_ok(qkv_dtype) || !dtype_ok(la_dtype) || !dtype_ok(beta_dtype)) return -1;
   const int units = N * H;
   int failed = 0;
 #pragma omp parallel for schedule(static)
   for (int unit = 0; unit < units; ++unit) {
     const int n = unit / H, h = unit % H;
-    double* buf = (double*)malloc(sizeof(double) * (size_t)(3 * dk + 3 * dv));
+    double* buf = (double*)malloc(sizeof(double) * (size_t)(3 * dk + 3 * dv + 9 * dk));
     if (!buf) {
 #pragma omp atomic write
       failed = 1;
       continue;
     }
     double *qd = buf, *kd = buf + dk, *lad = buf + 2 * dk;
-    double *vd = buf + 3 * dk, *u = vd + dv, *ot = u + dv;
+    double *vd = buf + 3 * dk, *u = vd + dv, *ot = u + dv, *hist = ot + dv;
     double b;
+    if (opt->conv_weight) init_hist(hist, conv_state, n, H, h, dk);
     prologue(q, k, v, qkv_dtype, log_alpha, la_dtype, beta, beta_dtype,
-             (size_t)n, H, h, dk, dv, opt, qd, kd, vd, lad, &b);
+             (size_t)n, H, h, dk, dv, opt, hist, qd, kd, vd, lad, &b);
+    if (opt->conv_weight && conv_state) store_hist(hist, conv_state, n, H, h, dk);
     token_step(S + (size_t)unit * dk * dv, dk, dv, qd, kd, vd, lad, b, opt, u, ot);
     memcpy(o + (size_t)unit * dv, ot, sizeof(double) * dv);
     free(buf);

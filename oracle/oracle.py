@@ -25,6 +25,10 @@ class _Opts(ctypes.Structure):
         ("g_min", ctypes.c_double),
         ("q_scale", ctypes.c_double),
         ("eps_l2", ctypes.c_double),
+        ("decay_from_logit", ctypes.c_int),
+        ("decay_scale", ctypes.c_void_p),
+        ("decay_bias", ctypes.c_void_p),
+        ("conv_weight", ctypes.c_void_p),
     ]
 
 
@@ -80,11 +84,11 @@ class Oracle:
         vp, ci, cd = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         lib.kda_oracle_prefill.argtypes = [vp, vp, vp, ci, vp, ci, vp, ci, vp, vp,
                                            ci, ci, ci, ci, ci, ci, ci,
-                                           ctypes.POINTER(_Opts), vp, vp]
+                                           ctypes.POINTER(_Opts), vp, vp, vp]
         lib.kda_oracle_prefill.restype = ci
         lib.kda_oracle_decode_step.argtypes = [vp, vp, vp, ci, vp, ci, vp, ci, vp,
                                                ci, ci, ci, ci,
-                                               ctypes.POINTER(_Opts), vp]
+                                               ctypes.POINTER(_Opts), vp, vp]
         lib.kda_oracle_decode_step.restype = ci
         lib.kda_oracle_gated_rmsnorm.argtypes = [vp, ci, ci, ci, vp, ci, ci, ci,
                                                  vp, cd, vp]
@@ -94,21 +98,34 @@ class Oracle:
         self.mutation = lib.kda_oracle_mutation()
 
     @staticmethod
-    def _opts(l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2):
-        return _Opts(int(bool(l2norm_qk)), int(bool(beta_is_logit)), float(g_min),
-                     float(q_scale), float(eps_l2))
+    def _opts(l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2, decay_from_logit=False,
+              decay_scale=None, decay_bias=None, conv_weight=None):
+        """The options struct and the fp64 arrays it points to (keep both alive
+        for the call)."""
+        keep = [None if a is None else _f64(a) for a in (decay_scale, decay_bias, conv_weight)]
+        opts = _Opts(int(bool(l2norm_qk)), int(bool(beta_is_logit)), float(g_min),
+                     float(q_scale), float(eps_l2), int(bool(decay_from_logit)),
+                     *[None if a is None else a.ctypes.data for a in keep])
+        return opts, keep
 
     def prefill(self, q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, *,
                 N: int | None = None, heads: tuple[int, int] | None = None,
                 l2norm_qk: bool = True, beta_is_logit: bool = False,
                 g_min: float = -5.0, q_scale: float = 1.0, eps_l2: float = 1e-6,
-                want_state: bool = True):
+                decay_from_logit: bool = False, decay_scale=None, decay_bias=None,
+                conv_weight=None, conv_state=None, want_state: bool = True):
         """Token-by-token prefill.
 
         Shapes: q, k, log_alpha [T, H, dk]; v [T, H, dv]; beta [T, H];
         S0 [N, H, dk, dv] (or None = zeros); cu_seqlens [N+1] int (or None = N
         equal sequences, N defaults to 1).  ``heads`` = (h0, nh) restricts the
-        computation to a head range.  Returns (o [T, nh, dv], S_T [N, nh, dk, dv]).
+        computation to a head range.  With ``decay_from_logit`` log_alpha holds
+        decay logits z and log alpha = g_min * sigmoid(A_h (z + b)), A =
+        ``decay_scale`` [H] (None = ones), b = ``decay_bias`` [H, dk] (None =
+        zeros).  ``conv_weight`` [3, H, d, 4] turns on the short convolution +
+        Swish of q, k, v, with ``conv_state`` [N, 3, 3, H, d] the raw rows
+        before each sequence (None = zeros).  Returns (o [T, nh, dv],
+        S_T [N, nh, dk, dv]).
         """
         qa, qd = _as_buffer(q)
         ka, kd_ = _as_buffer(k)
@@ -130,21 +147,28 @@ class Oracle:
             cu, cu_p = None, None
         h0, nh = heads if heads is not None else (0, H)
         s0 = _f64(S0) if S0 is not None else None
+        cs = _f64(conv_state) if conv_state is not None else None
         o = np.empty((T, nh, dv), dtype=np.float64)
         st = np.empty((N, nh, dk, dv), dtype=np.float64) if want_state else None
-        opts = self._opts(l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2)
+        opts, keep = self._opts(l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+                                decay_from_logit, decay_scale, decay_bias, conv_weight)
         rc = self.lib.kda_oracle_prefill(
             _ptr(qa), _ptr(ka), _ptr(va), qd, _ptr(la), lad, _ptr(ba), bd,
             _ptr(s0) if s0 is not None else None, cu_p, N, T, H, dk, dv, h0, nh,
-            ctypes.byref(opts), _ptr(o), _ptr(st) if st is not None else None)
+            ctypes.byref(opts), _ptr(o), _ptr(st) if st is not None else None,
+            _ptr(cs) if cs is not None else None)
+        del keep
         if rc != 0:
             raise ValueError("oracle: kda_oracle_prefill rejected its arguments")
         return o, st
 
     def decode_step(self, q, k, v, log_alpha, beta, S, *, l2norm_qk=True,
-                    beta_is_logit=False, g_min=-5.0, q_scale=1.0, eps_l2=1e-6):
+                    beta_is_logit=False, g_min=-5.0, q_scale=1.0, eps_l2=1e-6,
+                    decay_from_logit=False, decay_scale=None, decay_bias=None,
+                    conv_weight=None, conv_state=None):
         """One recurrent step for N sequences.  S [N, H, dk, dv] is NOT modified;
-        returns (o [N, H, dv], S_new [N, H, dk, dv])."""
+        returns (o [N, H, dv], S_new [N, H, dk, dv]), and with ``conv_weight``
+        (o, S_new, conv_state_new [N, 3, 3, H, d]) (``conv_state`` None = zeros)."""
         qa, qd = _as_buffer(q)
         ka, _ = _as_buffer(k)
         va, _ = _as_buffer(v)
@@ -154,12 +178,21 @@ class Oracle:
         dv = va.shape[2]
         s = _f64(S).copy()
         o = np.empty((N, H, dv), dtype=np.float64)
-        opts = self._opts(l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2)
+        cs = None
+        if conv_weight is not None:
+            cs = (_f64(conv_state).copy() if conv_state is not None
+                  else np.zeros((N, 3, 3, H, dk), dtype=np.float64))
+        opts, keep = self._opts(l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
+                                decay_from_logit, decay_scale, decay_bias, conv_weight)
         rc = self.lib.kda_oracle_decode_step(
             _ptr(qa), _ptr(ka), _ptr(va), qd, _ptr(la), lad, _ptr(ba), bd,
-            _ptr(s), N, H, dk, dv, ctypes.byref(opts), _ptr(o))
+            _ptr(s), N, H, dk, dv, ctypes.byref(opts), _ptr(o),
+            _ptr(cs) if cs is not None else None)
+        del keep
         if rc != 0:
             raise ValueError("oracle: kda_oracle_decode_step rejected its arguments")
+        if conv_weight is not None:
+            return o, s, cs
         return o, s
 
     def gated_rmsnorm(self, o, gate, w=None, eps: float = 1e-6, h0: int = 0):

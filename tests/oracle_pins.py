@@ -464,6 +464,152 @@ def pin_input_widening(orc):
         np.testing.assert_array_equal(orc.gated_rmsnorm(o1, gin), orc.gated_rmsnorm(o1, gref))
 
 
+# ---------------------------------------------------------------- decay from logits
+def _retention(orc, z, *, A=None, b=None, g_min=-5.0):
+    """exp(log alpha) for decay logits z [d] (one head per channel reads its
+    channel of S0 = I after one step with beta = 0)."""
+    d = z.shape[-1]
+    H = d
+    eye = np.eye(d)
+    q = np.broadcast_to(eye[None], (1, H, d)).copy()       # head h reads channel h
+    zero = np.zeros((1, H, d))
+    la = np.broadcast_to(z, (1, H, d)).copy()
+    S0 = np.broadcast_to(eye, (1, H, d, d)).copy()
+    Ah = None if A is None else np.full(H, float(A))
+    bh = None if b is None else np.broadcast_to(b, (H, d)).copy()
+    o, _ = orc.prefill(q, zero, zero, la, np.zeros((1, H)), S0, l2norm_qk=False, eps_l2=0.0,
+                       decay_from_logit=True, decay_scale=Ah, decay_bias=bh, g_min=g_min)
+    return np.diagonal(o[0])
+
+
+def pin_decay_logit(orc):
+    """log alpha from the decay logit z through the bounded sigmoid with one
+    scale A_h per head: every factor lies in [e^g_min, 1] whatever z is, the
+    extremes are reached as z -> +-inf, z + b = 0 gives exactly half the
+    floor, larger z forgets more, A_h scales the logit inside the sigmoid,
+    the per-channel bias adds to z, and A_h = 1, b = 0 reproduces the plain
+    path fed log alpha = -5 sigmoid(z)."""
+    z = np.array([1e3, -1e3, 0.0, 2.0, -2.0, 40.0])
+    a = _retention(orc, z)
+    assert a[0] == math.exp(-5.0) and a[1] == 1.0
+    assert a[2] == math.exp(-2.5)
+    a2 = _retention(orc, z, g_min=-2.0)
+    assert a2[0] == math.exp(-2.0) and a2[1] == 1.0 and a2[2] == math.exp(-1.0)
+    r = _rng(41)
+    zz = np.sort(r.uniform(-50.0, 50.0, size=16))
+    aa = _retention(orc, zz)
+    assert np.all(aa >= math.exp(-5.0)) and np.all(aa <= 1.0)
+    assert np.all(np.diff(aa) <= 0.0)                   # monotone: more forgetting
+    x = r.normal(size=8)
+    np.testing.assert_array_equal(_retention(orc, x, A=2.0), _retention(orc, 2.0 * x))
+    y = r.normal(size=8)
+    np.testing.assert_array_equal(_retention(orc, x, b=y), _retention(orc, x + y))
+    # the full recurrence: logits in, the same as the activated log alpha in
+    T, H, d = 9, 2, 8
+    q, k, v = r.normal(size=(T, H, d)), r.normal(size=(T, H, d)), r.normal(size=(T, H, d))
+    zt = r.normal(size=(T, H, d)) * 1.5
+    bt = r.uniform(0.1, 1.0, size=(T, H))
+    o1, s1 = orc.prefill(q, k, v, zt, bt, decay_from_logit=True)
+    o2, s2 = orc.prefill(q, k, v, -5.0 / (1.0 + np.exp(-zt)), bt)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(s1, s2, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- short convolution
+def _swish(y):
+    return y / (1.0 + np.exp(-y))
+
+
+def pin_short_conv_impulse(orc):
+    """A unit impulse through the width-4 causal convolution + Swish returns
+    swish(tap x height) at the impulse and the three tokens after it, oldest
+    tap last, and exactly zero before it and from four tokens on (a
+    constant key overwritten with beta = 1 reads back v's output)."""
+    T, d, t0 = 10, 4, 2
+    r = _rng(43)
+    w = r.normal(size=(3, 1, d, 4))
+    w[0, 0] = w[1, 0] = [0.0, 0.0, 0.0, 1.0]         # q, k: identity taps
+    e0 = np.zeros((T, 1, d))
+    e0[:, 0, 0] = 1.0
+    heights = np.array([0.5, -1.25, 2.0, 0.75])
+    v = np.zeros((T, 1, d))
+    v[t0, 0] = heights
+    o, _ = orc.prefill(e0, e0, v, np.zeros((T, 1, d)), np.ones((T, 1)), eps_l2=0.0,
+                       conv_weight=w)
+    want = np.zeros((T, d))
+    for t in range(t0, t0 + 4):
+        want[t] = _swish(w[2, 0, :, 3 - (t - t0)] * heights)
+    np.testing.assert_allclose(o[:, 0], want, rtol=1e-14, atol=1e-15)
+    # the query's convolution, read through S0 = I with beta = 0 (no norm)
+    q = np.zeros((T, 1, d))
+    q[t0, 0] = heights
+    o, _ = orc.prefill(q, np.zeros((T, 1, d)), np.zeros((T, 1, d)), np.zeros((T, 1, d)),
+                       np.zeros((T, 1)), np.eye(d)[None, None], l2norm_qk=False,
+                       conv_weight=np.repeat(w[2:3], 3, axis=0))
+    np.testing.assert_allclose(o[:, 0], want, rtol=1e-14, atol=1e-15)
+
+
+def _conv_ref(x, w, window):
+    """Causal conv of x [T, H, d] with taps w [H, d, 4] (oldest first) after the
+    window [3, H, d], by numpy.convolve per channel, then Swish."""
+    T, H, d = x.shape
+    full = np.concatenate([window, x], axis=0)
+    y = np.empty_like(x)
+    for h in range(H):
+        for c in range(d):
+            y[:, h, c] = np.convolve(full[:, h, c], w[h, c, ::-1])[3:3 + T]
+    return _swish(y)
+
+
+def pin_short_conv(orc):
+    """Convolution + Swish on q, k and v equals the plain recurrence on inputs
+    convolved by numpy.convolve (after the caller's window of earlier rows);
+    packed sequences each restart from their own window; a prefill split in
+    two (the second part given the first part's last three raw rows) and a
+    run of decode steps carrying the window give the same result."""
+    r = _rng(47)
+    T, H, d = 12, 2, 6
+    q, k, v = r.normal(size=(T, H, d)), r.normal(size=(T, H, d)), r.normal(size=(T, H, d))
+    la = r.uniform(-5, 0, size=(T, H, d))
+    b = r.uniform(0.1, 1, size=(T, H))
+    w = r.normal(size=(3, H, d, 4)) * 0.7
+    win = r.normal(size=(1, 3, 3, H, d))
+    S0 = r.normal(size=(1, H, d, d))
+    o, S_T = orc.prefill(q, k, v, la, b, S0, conv_weight=w, conv_state=win, eps_l2=0.0)
+    qc, kc, vc = (_conv_ref(x, w[i], win[0, i]) for i, x in enumerate((q, k, v)))
+    o2, S2 = orc.prefill(qc, kc, vc, la, b, S0, eps_l2=0.0)
+    np.testing.assert_allclose(o, o2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(S_T, S2, rtol=1e-12, atol=1e-12)
+    # packed: each sequence from its own window
+    T1 = 5
+    cu = np.array([0, T1, T], dtype=np.int32)
+    win2 = r.normal(size=(2, 3, 3, H, d))
+    S02 = r.normal(size=(2, H, d, d))
+    op, Sp = orc.prefill(q, k, v, la, b, S02, cu, conv_weight=w, conv_state=win2, eps_l2=0.0)
+    oa, Sa = orc.prefill(q[:T1], k[:T1], v[:T1], la[:T1], b[:T1], S02[:1], conv_weight=w,
+                         conv_state=win2[:1], eps_l2=0.0)
+    ob, Sb = orc.prefill(q[T1:], k[T1:], v[T1:], la[T1:], b[T1:], S02[1:], conv_weight=w,
+                         conv_state=win2[1:], eps_l2=0.0)
+    np.testing.assert_array_equal(op, np.concatenate([oa, ob]))
+    np.testing.assert_array_equal(Sp, np.concatenate([Sa, Sb]))
+    # split: the second part's window is the first part's last three raw rows
+    oa, Sa = orc.prefill(q[:T1], k[:T1], v[:T1], la[:T1], b[:T1], S0, conv_weight=w,
+                         conv_state=win, eps_l2=0.0)
+    tail = np.stack([x[T1 - 3:T1] for x in (q, k, v)])[None]
+    ob, Sb = orc.prefill(q[T1:], k[T1:], v[T1:], la[T1:], b[T1:], Sa, conv_weight=w,
+                         conv_state=tail, eps_l2=0.0)
+    np.testing.assert_allclose(np.concatenate([oa, ob]), o, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(Sb, S_T, rtol=1e-13, atol=1e-13)
+    # decode steps carry the window
+    S, cs = S0.copy(), win.copy()
+    for t in range(T):
+        ot, S, cs = orc.decode_step(q[t:t + 1], k[t:t + 1], v[t:t + 1], la[t:t + 1], b[t:t + 1],
+                                    S, conv_weight=w, conv_state=cs, eps_l2=0.0)
+        np.testing.assert_allclose(ot[0], o[t], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(S, S_T, rtol=1e-13, atol=1e-13)
+    np.testing.assert_array_equal(cs[0], np.stack([x[T - 3:] for x in (q, k, v)]))
+
+
 ALL_PINS = [
     pin_brute_force,
     pin_overwrite,
@@ -477,4 +623,7 @@ ALL_PINS = [
     pin_split_and_decode,
     pin_gated_rmsnorm,
     pin_input_widening,
+    pin_decay_logit,
+    pin_short_conv_impulse,
+    pin_short_conv,
 ]

@@ -5,7 +5,9 @@ mathematics.  The faithful build must pass every pin; each build with a planted
 mistake (a dropped fade, a read before the write, a wrong sign, a wrong index,
 a dropped beta, a missing floor, the fade in the wrong place, a missing key
 normalisation, the wrong probe vector, a wrong widening of bf16 or fp32
-inputs) must fail at least one of them.  A marshalling mistake on the Python
+inputs, reversed convolution taps or window, a missing Swish, a convolution
+across a sequence boundary, an unbounded or mis-scaled decay mapping) must
+fail at least one of them.  A marshalling mistake on the Python
 side (bf16 passed through float16) is planted the same way.
 """
 import os
@@ -28,6 +30,12 @@ MUTATIONS = {
     9: "state probed with the query",
     10: "bf16 input widened with the wrong shift",
     11: "fp32 input cut to bf16",
+    12: "convolution taps applied newest first",
+    13: "no Swish on v",
+    14: "decay logit through the old unbounded softplus",
+    15: "decay scale outside the sigmoid",
+    16: "convolution window read newest first",
+    17: "convolution reads across a packed-sequence boundary",
 }
 
 
