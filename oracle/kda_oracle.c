@@ -16,7 +16,15 @@
  *      through a short convolution of width 4, Swish and L2 normalisation,
  *      values through the convolution and Swish).  Taps w[c][0..3] weigh the
  *      raw rows t-3 .. t, oldest first; rows before the sequence start are
- *      the caller's window of earlier rows, zeros by default.
+ *      the caller's window of earlier rows, zeros by default.  The
+ *      convolution is the layer before the recurrence: its output is held in
+ *      the data type of q, k, v (rounded to nearest-even bf16 for bf16 data,
+ *      fp32 for fp32 data), as it would be when handed over by a separate
+ *      convolution layer; from there on the arithmetic is fp64.  Storing is a
+ *      quantisation, so for bf16 and fp32 data the value being stored is
+ *      computed in the precision of the CUDA kernels: fp32, one fixed order of
+ *      operations, and an exponential made of IEEE operations only (see
+ *      conv_swish_f32).  fp64 data keeps an fp64 convolution and no rounding.
  *   1. q <- q / sqrt(sum q^2 + eps), k likewise (optional; the layer applies
  *      L2 normalisation to queries and keys: "Kimi K3's hybrid block, from
  *      first principles", section "From linear attention to the delta rule").
@@ -211,30 +219,93 @@ static void token_step(double* S, int dk, int dv, const double* q,
 
 static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+/* x held in storage type `dtype`: fp32 by the C conversion (round to nearest),
+ * bf16 by rounding that binary32 pattern to its upper 16 bits, to nearest
+ * with ties to even; fp64 unchanged. */
+static double store_as(double x, int dtype) {
+  if (dtype == ORC_F64) return x;
+  float f = (float)x;
+  if (dtype == ORC_BF16) {
+    uint32_t b;
+    memcpy(&b, &f, sizeof b);
+#if KDA_ORACLE_MUTATION != 18
+    b += 0x7FFFu + ((b >> 16) & 1u);
+#endif
+    b &= 0xFFFF0000u; /* (mutation 18 plants truncation instead of rounding) */
+    memcpy(&f, &b, sizeof f);
+  }
+  return (double)f;
+}
+
+/* e^t for fp32 t in [-80, 80] from IEEE operations only, so that any
+ * implementation of the same steps gets the same bits: Cody and Waite's range
+ * reduction t = n ln2 + r (n = rint(t log2 e), ln2 split into a 14-bit head,
+ * exact in n * head, and a tail), then the Taylor polynomial of e^r to degree
+ * 6 (|r| <= 0.35) by Horner's rule, scaled by 2^n. */
+static float exp_f32(float t) {
+  const float n = rintf(t * 0x1.715476p+0f);
+  float r = fmaf(-n, 0x1.62e4p-1f, t);
+  r = fmaf(-n, 0x1.7f7d1cp-20f, r);
+  float p = 0x1.6c16c2p-10f;     /* 1/720 */
+  p = fmaf(p, r, 0x1.111112p-7f); /* 1/120 */
+  p = fmaf(p, r, 0x1.555556p-5f); /* 1/24  */
+  p = fmaf(p, r, 0x1.555556p-3f); /* 1/6   */
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  return ldexpf(p, (int)n);
+}
+
+/* The stored value of the convolution + Swish in fp32 (the kernels'
+ * precision): y = w3 x3 + w2 x2 + w1 x1 + w0 x0 accumulated in that order by
+ * fused multiply-adds (x0 the oldest row), then y * sigmoid(y) with
+ * sigmoid(y) = 1 / (1 + e^-y), the exponent clamped to [-80, 80]. */
+static float conv_swish_f32(const double* wc, const double* xs) {
+  const float w0 = (float)wc[0], w1 = (float)wc[1], w2 = (float)wc[2], w3 = (float)wc[3];
+  float y = w3 * (float)xs[3];
+  y = fmaf(w2, (float)xs[2], y);
+  y = fmaf(w1, (float)xs[1], y);
+  y = fmaf(w0, (float)xs[0], y);
+  float t = -y;
+  t = t < -80.0f ? -80.0f : (t > 80.0f ? 80.0f : t);
+  const float sg = 1.0f / (1.0f + exp_f32(t));
+  return y * sg;
+}
+
 /* Step 0 for one tensor X (0 = q, 1 = k, 2 = v) of one (token, head h of H):
  * x holds the raw row and receives conv + Swish; the raw row enters the
  * history. */
-static void conv_swish(double* x, int X, int H, int h, int d, const kda_oracle_opts* opt,
-                       double* hist) {
+static void conv_swish(double* x, int X, int H, int h, int d, int dtype,
+                       const kda_oracle_opts* opt, double* hist) {
   double* hx = hist + (size_t)X * CONV_HIST * d;
   for (int c = 0; c < d; ++c) {
-    const double* wc = opt->conv_weight + (((size_t)X * H + h) * d + c) * CONV_W;
-    double y = 0.0;
+    const double* wc0 = opt->conv_weight + (((size_t)X * H + h) * d + c) * CONV_W;
+    /* the taps in the order they weigh the rows: oldest row first */
+    double wc[CONV_W];
+    for (int j = 0; j < CONV_W; ++j) {
 #if KDA_ORACLE_MUTATION == 12
-    /* planted mistake: taps applied newest row first */
-    for (int j = 0; j < CONV_HIST; ++j) y += wc[CONV_W - 1 - j] * hx[(size_t)j * d + c];
-    y += wc[0] * x[c];
+      wc[j] = wc0[CONV_W - 1 - j]; /* planted mistake: taps applied newest row first */
 #else
-    for (int j = 0; j < CONV_HIST; ++j) y += wc[j] * hx[(size_t)j * d + c];
-    y += wc[CONV_W - 1] * x[c];
+      wc[j] = wc0[j];
 #endif
+    }
+    const double xs[CONV_W] = {hx[c], hx[(size_t)d + c], hx[(size_t)2 * d + c], x[c]};
     for (int j = 0; j + 1 < CONV_HIST; ++j) hx[(size_t)j * d + c] = hx[(size_t)(j + 1) * d + c];
     hx[(size_t)(CONV_HIST - 1) * d + c] = x[c];
 #if KDA_ORACLE_MUTATION == 13
-    x[c] = (X == 2) ? y : y * sigmoid(y); /* planted mistake: no Swish on v */
+    const int swish = X != 2; /* planted mistake: no Swish on v */
 #else
-    x[c] = y * sigmoid(y);
+    const int swish = 1;
 #endif
+    if (dtype == ORC_F64) {
+      double y = 0.0;
+      for (int j = 0; j < CONV_W; ++j) y += wc[j] * xs[j];
+      x[c] = swish ? y * sigmoid(y) : y;
+    } else if (swish) {
+      x[c] = store_as((double)conv_swish_f32(wc, xs), dtype);
+    } else {
+      x[c] = store_as(wc[3] * xs[3] + wc[2] * xs[2] + wc[1] * xs[1] + wc[0] * xs[0], dtype);
+    }
   }
 }
 
@@ -255,9 +326,9 @@ static void prologue(const void* q, const void* k, const void* v, int qkv_dtype,
   }
   for (int j = 0; j < dv; ++j) vd[j] = load_elem(v, qkv_dtype, v_off + j);
   if (opt->conv_weight) {
-    conv_swish(qd, 0, H, h, dk, opt, hist);
-    conv_swish(kd, 1, H, h, dk, opt, hist);
-    conv_swish(vd, 2, H, h, dv, opt, hist);
+    conv_swish(qd, 0, H, h, dk, qkv_dtype, opt, hist);
+    conv_swish(kd, 1, H, h, dk, qkv_dtype, opt, hist);
+    conv_swish(vd, 2, H, h, dv, qkv_dtype, opt, hist);
   }
   if (opt->decay_from_logit) {
     const double A = opt->decay_scale ? opt->decay_scale[h] : 1.0;

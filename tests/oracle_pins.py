@@ -561,6 +561,53 @@ def _conv_ref(x, w, window):
     return _swish(y)
 
 
+def _held_q(orc, q, w, win):
+    """The stored convolution + Swish output of q, read back exactly: with
+    S0 = I, beta = 0, no decay and no norm, o_t = the stored q_t."""
+    T, H, d = q.shape
+    z = q * 0                                  # k, v: zeros of q's storage type
+    S0 = np.broadcast_to(np.eye(d), (1, H, d, d)).copy()
+    o, _ = orc.prefill(q, z, z, np.zeros((T, H, d)), np.zeros((T, H)), S0, l2norm_qk=False,
+                       conv_weight=w, conv_state=win)
+    return o
+
+
+def pin_short_conv_storage(orc):
+    """With bf16 (fp32) data the convolution's output is held in bf16 (fp32)
+    before the rest of the layer, rounded to nearest even.  Against the fp64
+    convolution + Swish by numpy.convolve: every stored bf16 value is that
+    value rounded to nearest bf16 by the library's conversion, except where it
+    lies within the fp32 evaluation error of a rounding boundary (then either
+    neighbour); every stored fp32 value is within that evaluation error of it
+    (relative 1e-6, plus 2e-6 absolute where the convolution's sum cancels)."""
+    import torch
+    r = _rng(53)
+    T, H, d = 40, 2, 16
+    g = torch.Generator().manual_seed(53)
+    q = (torch.randn((T, H, d), generator=g) * 2.0).to(torch.bfloat16)
+    w = r.normal(size=(3, H, d, 4)) * 0.7
+    win = (torch.randn((1, 3, 3, H, d), generator=g) * 2.0).to(torch.bfloat16)
+    true = _conv_ref(q.double().numpy(), w[0], win[0, 0].double().numpy())
+    held = _held_q(orc, q, w, win)
+    want = torch.from_numpy(true).float().bfloat16().double().numpy()
+    ok = held == want
+    # mismatches only next to a rounding boundary, and only by one bf16 unit
+    _, e = np.frexp(np.abs(true))
+    ulp = np.ldexp(1.0, e - 8)                 # bf16 spacing at |true| (8 significant bits)
+    # the fp32 evaluation error: relative, plus absolute where the sum cancels
+    near = np.abs(np.abs(true - want) - ulp / 2) <= 1e-5 * np.abs(true) + 2e-6
+    assert np.all(ok | near), f"{int((~(ok | near)).sum())} stored values off"
+    assert np.all(np.abs(held - want) <= ulp + 1e-300)
+    assert (~ok).sum() <= max(2, ok.size // 1000)
+    assert np.mean(held != true) > 0.9              # the rounding happened
+    # fp32 data: held in fp32
+    q32 = q.float().numpy()
+    held32 = _held_q(orc, q32, w, win.float().numpy())
+    true32 = _conv_ref(q32.astype(np.float64), w[0], win[0, 0].double().numpy())
+    np.testing.assert_allclose(held32, true32, rtol=1e-6, atol=2e-6)
+    assert np.all(held32 == held32.astype(np.float32))
+
+
 def pin_short_conv(orc):
     """Convolution + Swish on q, k and v equals the plain recurrence on inputs
     convolved by numpy.convolve (after the caller's window of earlier rows);
@@ -625,5 +672,6 @@ ALL_PINS = [
     pin_input_widening,
     pin_decay_logit,
     pin_short_conv_impulse,
+    pin_short_conv_storage,
     pin_short_conv,
 ]

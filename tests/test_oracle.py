@@ -36,6 +36,7 @@ MUTATIONS = {
     15: "decay scale outside the sigmoid",
     16: "convolution window read newest first",
     17: "convolution reads across a packed-sequence boundary",
+    18: "convolution output truncated to bf16 instead of rounded",
 }
 
 
