@@ -116,6 +116,28 @@ typedef struct kda_options {
                             T_total with them); slot m of sequence n holds
                             the state after (m + 1) * snapshot_every of its
                             tokens, slots past its length are not written   */
+  /* The prologue from raw projections ("Kimi K3's hybrid block, from first
+   * principles", section "From linear attention to the delta rule"; section
+   * "What changed": the decay mapping became a bounded sigmoid). */
+  int decay_from_logit;  /* 0 (default): log_alpha holds log decays.  1: it holds
+                            the decay logits z [T][H][d_k] (KDA_DECAY_CHANNEL
+                            only) and log alpha = g_min * sigmoid(A_h (z + b))  */
+  const float* decay_scale; /* with decay_from_logit: A [H] fp32, NULL = ones   */
+  const float* decay_bias;  /* with decay_from_logit: b [H][d_k] fp32, NULL = 0 */
+  const float* conv_weight; /* NULL (default): q, k, v are used as given.  Else
+                            fp32 [3 (q, k, v)][H][d][4], 16-byte aligned: each
+                            of q, k, v first passes through a causal depthwise
+                            convolution of width 4 over the tokens of its
+                            sequence (tap 0 weighs the row 3 tokens back, tap 3
+                            the token's own row), then Swish x * sigmoid(x);
+                            q and k are L2-normalised after that            */
+  void* conv_state;      /* with conv_weight: the raw q, k, v rows of the 3
+                            tokens before each sequence, [N][3 (q, k, v)][3
+                            (oldest first)][H][d] (dtype), 16-byte aligned;
+                            NULL = zeros.  kda_prefill only reads it (after a
+                            prefill, the next window is the last 3 raw rows
+                            of the sequence); kda_decode_step reads it and
+                            writes the window that ends with this token      */
 } kda_options;
 
 /* Fill *opt with the defaults listed above. */

@@ -98,6 +98,13 @@ int check_common_opts(const kda_options* o) {
   if (o->decay_mode < KDA_DECAY_CHANNEL || o->decay_mode > KDA_DECAY_NONE) return KDA_ERR_ARG;
   if (o->gate && !aligned16(o->gate)) return KDA_ERR_ALIGN;
   if (o->norm_weight && !aligned16(o->norm_weight)) return KDA_ERR_ALIGN;
+  if (o->decay_from_logit != 0 && o->decay_from_logit != 1) return KDA_ERR_ARG;
+  if (o->decay_from_logit && o->decay_mode != KDA_DECAY_CHANNEL) return KDA_ERR_ARG;
+  if ((o->decay_scale && (reinterpret_cast<uintptr_t>(o->decay_scale) & 3u)) ||
+      (o->decay_bias && (reinterpret_cast<uintptr_t>(o->decay_bias) & 3u)))
+    return KDA_ERR_ALIGN;
+  if (o->conv_weight && !aligned16(o->conv_weight)) return KDA_ERR_ALIGN;
+  if (o->conv_state && !aligned16(o->conv_state)) return KDA_ERR_ALIGN;
   return KDA_OK;
 }
 
@@ -175,7 +182,7 @@ void kda_options_init(kda_options* opt) {
   opt->decay_mode = KDA_DECAY_CHANNEL;
 }
 
-int kda_abi_version(void) { return 2; }
+int kda_abi_version(void) { return 3; }
 
 const char* kda_status_string(int s) {
   switch (s) {
@@ -245,6 +252,11 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* log_al
   a.snapshots = snap_slots > 0 ? op->snapshots : nullptr;
   a.snapshot_every = op->snapshot_every;
   a.snapshot_slots = snap_slots;
+  a.decay_from_logit = op->decay_from_logit;
+  a.decay_scale = op->decay_scale;
+  a.decay_bias = op->decay_bias;
+  a.conv_weight = op->conv_weight;
+  a.conv_state = op->conv_weight ? op->conv_state : nullptr;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
@@ -289,6 +301,11 @@ int kda_decode_step(const void* q, const void* k, const void* v, const float* lo
   a.decay_mode = op->decay_mode;
   a.g_min = op->g_min; a.q_scale = op->q_scale; a.eps_l2 = op->eps_l2;
   a.eps_norm = op->eps_norm;
+  a.decay_from_logit = op->decay_from_logit;
+  a.decay_scale = op->decay_scale;
+  a.decay_bias = op->decay_bias;
+  a.conv_weight = op->conv_weight;
+  a.conv_state = op->conv_weight ? op->conv_state : nullptr;
   cudaError_t e = launch_decode(a, dtype, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

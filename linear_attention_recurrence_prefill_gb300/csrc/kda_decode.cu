@@ -47,14 +47,47 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
   const size_t base = (size_t)unit * D;
   // every global load of the token (and beta) is issued before the first barrier
   float qv = 0.f, kv = 0.f, vv = 0.f, lav = 0.f, bv = 0.f;
+  float win[3][3];  // short convolution: raw rows of the 3 previous tokens
+  float4 cw[3];     // and this channel's taps
+  T* cs = static_cast<T*>(a.conv_state);
+  const int n = unit / a.H, h = unit - n * a.H;
   if (tid < D) {
     qv = to_f32(q[base + tid]);
     kv = to_f32(k[base + tid]);
     vv = to_f32(v[base + tid]);
     lav = log_alpha_at(a.log_alpha, a.decay_mode, (size_t)unit, D, tid);
+    if (a.conv_weight) {
+#pragma unroll
+      for (int X = 0; X < 3; ++X) {
+        cw[X] = *reinterpret_cast<const float4*>(a.conv_weight +
+                                                 (((size_t)X * a.H + h) * D + tid) * 4);
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+          win[X][j] = cs ? to_f32(cs[(((size_t)n * 9 + X * 3 + j) * a.H + h) * D + tid]) : 0.f;
+      }
+    }
   }
   if (tid == 0) bv = to_f32(static_cast<const T*>(a.beta)[unit]);
   if (tid < D) {
+    if (a.conv_weight) {  // conv over (3 previous rows, this row), then Swish,
+      const float raw[3] = {qv, kv, vv};  // held in the data type
+      float y[3];
+#pragma unroll
+      for (int X = 0; X < 3; ++X) {
+        y[X] = to_f32(from_f32<T>(conv4_swish(cw[X], win[X][0], win[X][1], win[X][2], raw[X])));
+        if (cs) {  // the window that ends with this token
+          const size_t wb = ((size_t)n * 9 + X * 3) * a.H + h;
+          cs[(wb + 0 * (size_t)a.H) * D + tid] = from_f32<T>(win[X][1]);
+          cs[(wb + 1 * (size_t)a.H) * D + tid] = from_f32<T>(win[X][2]);
+          cs[(wb + 2 * (size_t)a.H) * D + tid] = from_f32<T>(raw[X]);
+        }
+      }
+      qv = y[0];
+      kv = y[1];
+      vv = y[2];
+    }
+    if (a.decay_from_logit)
+      lav = log_alpha_from_logit(lav, a.decay_scale, a.decay_bias, h, D, tid, a.g_min);
     sq[tid] = qv;
     sk[tid] = kv;
     sv[tid] = vv;

@@ -47,7 +47,9 @@ struct SimtSmem {  // offsets in floats
   static constexpr int beta = Tm + kC * kC; // [C]
   static constexpr int gam = beta + kC;     // [D]     G_C
   static constexpr int red = gam + D;       // [warps][C] partial sums of squares
-  static constexpr int total = red + (kThreads / 32) * kC;
+  static constexpr int hist = red + (kThreads / 32) * kC;  // [3][3][D] raw rows before
+                                            // the chunk (short convolution), oldest first
+  static constexpr int total = hist + 9 * D;
 };
 
 template <int D, typename T>
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillArgs a) {
   float* sbeta = sm + L::beta;
   float* sgam = sm + L::gam;
   float* red = sm + L::red;
+  float* hist = sm + L::hist;
 
   constexpr int RG = kThreads / D;  // row groups in the C x D work split
   constexpr int RPT = kC / RG;      // chunk rows per thread
@@ -100,6 +103,21 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillArgs a) {
   const int col = tid % D;
   const int grp = tid / D;
 
+  // short convolution: taps of this thread's column (the same column in every
+  // one of its chunk elements, since kThreads is a multiple of D), and the raw
+  // rows before the sequence
+  constexpr int E = kC * D / kThreads;  // chunk elements per thread
+  float4 cw[3];
+  if (a.conv_weight) {
+    for (int X = 0; X < 3; ++X)
+      cw[X] = *reinterpret_cast<const float4*>(a.conv_weight + (((size_t)X * H + h) * D + col) * 4);
+    const T* cs = static_cast<const T*>(a.conv_state);
+    for (int e = tid; e < 9 * D; e += kThreads) {  // e = (X * 3 + j) * D + c
+      const int Xj = e / D, c = e % D;
+      hist[e] = cs ? to_f32(cs[(((size_t)n * 9 + Xj) * H + h) * D + c]) : 0.f;
+    }
+  }
+
   for (int c0 = t0; c0 < t1; c0 += kC) {
     // 1. load the chunk (tokens past the sequence end are identity steps)
     for (int e = tid; e < kC * D; e += kThreads) {
@@ -111,8 +129,10 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillArgs a) {
         qv = to_f32(q[gi]);
         kv = to_f32(k[gi]);
         vv = to_f32(v[gi]);
-        la = fminf(fmaxf(log_alpha_at(a.log_alpha, a.decay_mode, (size_t)tok * H + h, D, c),
-                         a.g_min), 0.f);
+        la = log_alpha_at(a.log_alpha, a.decay_mode, (size_t)tok * H + h, D, c);
+        if (a.decay_from_logit)
+          la = log_alpha_from_logit(la, a.decay_scale, a.decay_bias, h, D, c, a.g_min);
+        la = fminf(fmaxf(la, a.g_min), 0.f);
       }
       Qt[e] = qv;
       Kt[e] = kv;
@@ -129,6 +149,43 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(PrefillArgs a) {
       sbeta[tid] = b;
     }
     __syncthreads();
+
+    // 1b. short convolution + Swish of q, k, v over the raw rows (the chunk's
+    //     and the three before it), the output held in the data type as a
+    //     separate convolution layer would hand it over; rows past the
+    //     sequence end stay identity steps whatever their values (beta = 0, no
+    //     decay)
+    if (a.conv_weight) {
+      float out[3][E], raw[3][E];
+      float* buf[3] = {Qt, Kt, Vb};
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int t = (tid + kThreads * i) / D;
+#pragma unroll
+        for (int X = 0; X < 3; ++X) {
+          float x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = t - 3 + j;
+            x[j] = r >= 0 ? buf[X][r * D + col] : hist[(X * 3 + 3 + r) * D + col];
+          }
+          raw[X][i] = x[3];
+          // held in the data type
+          out[X][i] = to_f32(from_f32<T>(conv4_swish(cw[X], x[0], x[1], x[2], x[3])));
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int t = (tid + kThreads * i) / D;
+#pragma unroll
+        for (int X = 0; X < 3; ++X) {
+          buf[X][t * D + col] = out[X][i];
+          if (t >= kC - 3) hist[(X * 3 + t - (kC - 3)) * D + col] = raw[X][i];
+        }
+      }
+      __syncthreads();
+    }
 
     // 2. L2 norms of q and k rows (one warp per row), running sum of log-decay
     if (a.l2norm_qk) {

@@ -190,7 +190,10 @@ static_assert(kTdW + 128 <= kPrepTmemCols, "W fits the TMEM allocation");
 constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
-constexpr uint32_t kPrepSmem = kPrepSmall + 3 * 64 * 4 + 1024;  // + alignment slack
+// short convolution: the raw q, k, v rows of the 3 tokens before the chunk,
+// bf16 [3 (q, k, v)][3][128] (unswizzled 256-byte rows)
+constexpr uint32_t kPrepHalo = kPrepSmall + 3 * 64 * 4;
+constexpr uint32_t kPrepSmem = kPrepHalo + 9 * 256 + 1024;  // + alignment slack
 static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reused region");
 static_assert(kPrepBl + 12288 <= kPrepSmall, "Gram operands inside the reused region");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
@@ -203,6 +206,14 @@ __device__ __forceinline__ float ex2f(float x) {  // hardware 2^x (rel. error ~2
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+__device__ __forceinline__ float rcpf(float x) {  // hardware 1/x (rel. error ~2^-23)
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// sigmoid(x) from the hardware 2^x and 1/x
+__device__ __forceinline__ float sigmoid_fast(float x) { return rcpf(1.f + ex2f(-kLog2e * x)); }
 
 __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
   const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&r);
@@ -281,6 +292,43 @@ __device__ __forceinline__ void split2v(float2 x, uint32_t& hi, uint32_t& lo) {
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// One row of the short convolution + Swish for 4 channels: taps w (oldest
+// first) over the window of the 3 previous raw rows and the raw row x (4 bf16
+// in a uint2); the window moves on by one row.  Returns the 4 outputs as bf16
+// pairs (rounded to nearest even: the value stored in the data type).
+__device__ __forceinline__ uint2 conv_row4(const float4 (&w)[4], float (&win)[3][4], uint2 raw) {
+  const float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u),
+                      __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xFFFF0000u)};
+  float y[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    y[c] = conv4_swish(w[c], win[0][c], win[1][c], win[2][c], x[c]);
+    win[0][c] = win[1][c];
+    win[1][c] = win[2][c];
+    win[2][c] = x[c];
+  }
+  return make_uint2(pack_bf162(y[0], y[1]), pack_bf162(y[2], y[3]));
+}
+
+__device__ __forceinline__ void unpack4(uint2 raw, float (&f)[4]) {
+  f[0] = __uint_as_float(raw.x << 16);
+  f[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(raw.y << 16);
+  f[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+}
+
+// taps of channels c0 .. c0 + 3 of tensor X (0 = q, 1 = k, 2 = v), head h
+__device__ __forceinline__ void conv_taps4(const float* cw, int X, int H, int h, int c0,
+                                           float4 (&w)[4]) {
+  const float4* p = reinterpret_cast<const float4*>(cw + (((size_t)X * H + h) * kD + c0) * 4);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = p[c];
+}
+
+// kConv: the short convolution runs in the prologue; kLogit: log alpha is
+// formed from decay logits.  Separate instantiations, so that the default one
+// carries none of their registers.
+template <bool kConv, bool kLogit>
 __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t bar_mma;
@@ -323,22 +371,42 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   // item's tokens follow by arithmetic, without a dependent load
   const int L_eq = a.cu_seqlens ? 0 : a.T_total / a.N;
   const int cps_eq = (L_eq + kC - 1) / kC;
-  auto decode = [&](int wi, int& gid_, int& h_, int& tok0_, int& len_) {
+  auto decode = [&](int wi, int& gid_, int& h_, int& tok0_, int& len_, int& n_, int& s0_) {
     h_ = wi / total;
     gid_ = wi - h_ * total;
     if (!a.cu_seqlens) {
-      const int n_ = gid_ / cps_eq;
-      tok0_ = n_ * L_eq + (gid_ - n_ * cps_eq) * kC;
+      n_ = gid_ / cps_eq;
+      s0_ = n_ * L_eq;
+      tok0_ = s0_ + (gid_ - n_ * cps_eq) * kC;
       len_ = min(kC, (n_ + 1) * L_eq - tok0_);
       return;
     }
-    const int n_ = find_seq(t.chunk_base, a.N, gid_);
-    int s0_, s1_;
+    n_ = find_seq(t.chunk_base, a.N, gid_);
+    int s1_;
     seq_range(a.cu_seqlens, a.N, a.T_total, n_, s0_, s1_);
     tok0_ = s0_ + (gid_ - t.chunk_base[n_]) * kC;
     len_ = min(kC, s1_ - tok0_);
   };
-  auto issue_inputs = [&](int h, int tok0, int len) {
+  auto issue_inputs = [&](int h, int tok0, int len, int n, int s0) {
+    // the raw q, k, v rows of the 3 tokens before the chunk (short convolution):
+    // from the token arrays inside the sequence, else from the caller's window
+    // (zeros without one)
+    if (kConv && tid < 144) {
+      const int X = tid / 48, j = (tid / 16) % 3, c16 = tid % 16;
+      const void* arr = X == 0 ? a.q : (X == 1 ? a.k : a.v);
+      const char* src;
+      uint32_t nbytes = 16u;
+      if (tok0 > s0) {
+        src = reinterpret_cast<const char*>(arr) + ((size_t)(tok0 - 3 + j) * H + h) * 256 + c16 * 16;
+      } else if (a.conv_state) {
+        src = reinterpret_cast<const char*>(a.conv_state) +
+              ((((size_t)n * 3 + X) * 3 + j) * H + h) * 256 + c16 * 16;
+      } else {
+        src = reinterpret_cast<const char*>(arr);
+        nbytes = 0u;
+      }
+      cp_async16(smem_u32(sm + kPrepHalo + (X * 3 + j) * 256 + c16 * 16), src, nbytes);
+    }
     // ---- 1. input rows by 16-byte asynchronous copies (all threads): q, k rows of
     //      256 B and log alpha rows of 512 B; rows past the sequence end are
     //      zero-filled (an identity step).  With one decay per head (or none) the
@@ -377,9 +445,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     }
   };
 
-  int item = blockIdx.x, gid, h, tok0, len;
-  decode(item, gid, h, tok0, len);
-  issue_inputs(h, tok0, len);
+  int item = blockIdx.x, gid, h, tok0, len, nseq, sstart;
+  decode(item, gid, h, tok0, len, nseq, sstart);
+  issue_inputs(h, tok0, len, nseq, sstart);
   uint32_t mma_phase = 0;
   bool ok = true;
   for (;;) {
@@ -388,6 +456,46 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     if (tid == 0) bulk_wait_read();  // the previous item's results have left region X
     __syncthreads();
 
+    // ---- 1b. short convolution + Swish of the q and k rows, in place: thread =
+    //      (tensor, 8-row block rb, 8-channel group c16) streams its rows through
+    //      a 3-row window; the 3 rows the next block still reads are written
+    //      after a barrier; the output is held in bf16, as a separate
+    //      convolution layer would hand it over ----
+    if constexpr (kConv) {
+      const int c16 = tid & 15, rb = (tid >> 4) & 7, X = tid >> 7;
+      uint8_t* rows = sm + (X ? kPrepK : kPrepQ);
+      const uint8_t* halo = sm + kPrepHalo + X * 3 * 256;
+      uint2 held[2][3];
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {  // the two 4-channel halves of the group
+        float4 w[4];
+        conv_taps4(a.conv_weight, X, a.H, h, 8 * c16 + 4 * hf, w);
+        float win[3][4];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const int r = 8 * rb - 3 + j;
+          const uint8_t* src = r >= 0 ? rows + r * 256 + rsw(r, c16) * 16 : halo + (3 + r) * 256 + c16 * 16;
+          unpack4(*reinterpret_cast<const uint2*>(src + 8 * hf), win[j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 8 * rb + i;
+          uint2* p = reinterpret_cast<uint2*>(rows + r * 256 + rsw(r, c16) * 16 + 8 * hf);
+          const uint2 y = conv_row4(w, win, *p);
+          if (i < 5) *p = y;
+          else held[hf][i - 5] = y;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 5; i < 8; ++i) {
+        const int r = 8 * rb + i;
+        *reinterpret_cast<uint4*>(rows + r * 256 + rsw(r, c16) * 16) =
+            make_uint4(held[0][i - 5].x, held[0][i - 5].y, held[1][i - 5].x, held[1][i - 5].y);
+      }
+      __syncthreads();
+    }
+
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
     //      registers); L2 norms of the q, k rows (warps 4-7, one row per thread) ----
     if (tid < kD) {  // thread tid scans float tid (as placed by gpos) of the rows
@@ -395,14 +503,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       // its latency
       float bt = 0.f;
       if (tid < len) bt = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
+      float dA = 1.f, db = 0.f;  // decay from logits: scale and this channel's bias
+      if constexpr (kLogit) {
+        const int ch = ((tid & 63) >> 2) * 8 + (tid >> 6) * 4 + (tid & 3);  // gpos^-1
+        if (a.decay_scale) dA = a.decay_scale[h];
+        if (a.decay_bias) db = a.decay_bias[(size_t)h * kD + ch];
+      }
       float x[kC];
 #pragma unroll
       for (int r = 0; r < kC; ++r) x[r] = G[gsw(r, tid)];
       float run = 0.f;
+      if constexpr (kLogit) {  // log alpha = g_min sigmoid(A (z + b)); rows past
+#pragma unroll                   // the sequence end stay at 0 (identity steps)
+        for (int r = 0; r < kC; ++r) {
+          const float la = r < len ? a.g_min * sigmoid_fast(dA * (x[r] + db)) : 0.f;
+          run += fminf(fmaxf(la, a.g_min), 0.f) * kLog2e;
+          x[r] = run;
+        }
+      } else {
 #pragma unroll
-      for (int r = 0; r < kC; ++r) {
-        run += fminf(fmaxf(x[r], a.g_min), 0.f) * kLog2e;
-        x[r] = run;
+        for (int r = 0; r < kC; ++r) {
+          run += fminf(fmaxf(x[r], a.g_min), 0.f) * kLog2e;
+          x[r] = run;
+        }
       }
 #pragma unroll
       for (int r = 0; r < kC; ++r) G[gsw(r, tid)] = x[r];
@@ -786,6 +909,38 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
             make_uint4(tl[0], tl[1], tl[2], tl[3]);
       }
       cp_async_wait_all();  // this thread's v rows have landed
+      if constexpr (kConv) {
+        // ---- 7b. short convolution + Swish of the v rows in place (MN-major
+        //      tile): thread = (4-row block, 8-channel group) ----
+        __syncthreads();  // every thread's v rows have landed
+        const int c16 = tid & 15, rb = tid >> 4;
+        const uint8_t* halo = sm + kPrepHalo + 2 * 3 * 256;
+        uint2 held[2][3];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float4 w[4];
+          conv_taps4(a.conv_weight, 2, a.H, h, 8 * c16 + 4 * hf, w);
+          float win[3][4];
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int r = 4 * rb - 3 + j;
+            const uint8_t* src = r >= 0 ? sm + kPrepV + sw128_chunk(r, c16, kC) : halo + (3 + r) * 256 + c16 * 16;
+            unpack4(*reinterpret_cast<const uint2*>(src + 8 * hf), win[j]);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint2* p = reinterpret_cast<uint2*>(sm + kPrepV + sw128_chunk(4 * rb + i, c16, kC) + 8 * hf);
+            const uint2 y = conv_row4(w, win, *p);
+            if (i == 0) *p = y;
+            else held[hf][i - 1] = y;
+          }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+          *reinterpret_cast<uint4*>(sm + kPrepV + sw128_chunk(4 * rb + i, c16, kC)) =
+              make_uint4(held[0][i - 1].x, held[0][i - 1].y, held[1][i - 1].x, held[1][i - 1].y);
+      }
       fence_proxy_async();
       fence_before_sync();
       __syncthreads();
@@ -818,10 +973,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       // the products are done with every buffer: the next item's inputs stream in
       // while this one's results leave TMEM
       const int w_next = item + (int)gridDim.x;
-      int gid_n = 0, h_n = 0, tok0_n = 0, len_n = 0;
+      int gid_n = 0, h_n = 0, tok0_n = 0, len_n = 0, n_n = 0, s0_n = 0;
       if (w_next < items) {
-        decode(w_next, gid_n, h_n, tok0_n, len_n);
-        issue_inputs(h_n, tok0_n, len_n);
+        decode(w_next, gid_n, h_n, tok0_n, len_n, n_n, s0_n);
+        issue_inputs(h_n, tok0_n, len_n, n_n, s0_n);
       }
       {
         // U~^T and W go to the free region X in the workspace's byte layout (U~^T:
@@ -872,6 +1027,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       h = h_n;
       tok0 = tok0_n;
       len = len_n;
+      nseq = n_n;
+      sstart = s0_n;
     }
   }
   goto done;
@@ -920,6 +1077,7 @@ static_assert(kChSmem <= 227 * 1024, "chain kernel shared memory");
 constexpr uint32_t kTS = 0, kTUO0 = 128, kTAS = 384, kTAU0 = 448;
 constexpr uint32_t kBarState = 1, kBarEpi = 2;  // named barriers of the two groups
 constexpr int kLoader = kChState;  // epilogue thread that issues the bulk loads
+
 
 // Hardware tanh (tanh.approx.f32, maximum relative error about 2^-11); the
 // gate uses sigmoid(x) = (1 + tanh(x / 2)) / 2, one MUFU operation per value.
@@ -1300,9 +1458,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
   if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPrepSmem);
-    if (e != cudaSuccess) return e;
+    for (auto kern : {prep_kernel<false, false>, prep_kernel<true, false>,
+                      prep_kernel<false, true>, prep_kernel<true, true>}) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kPrepSmem);
+      if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kChSmem);
     if (e != cudaSuccess) return e;
@@ -1316,8 +1477,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
     // persistent: two CTAs per SM walk the (chunk, head) items
     const long long items_max = (long long)t.total_chunks_max * a.H;
     const long long resident = 2LL * (dev >= 0 && dev < 64 ? sm_count[dev] : 148);
-    prep_kernel<<<(unsigned)(items_max < resident ? items_max : resident), kPrepThreads,
-                  kPrepSmem, s>>>(t);
+    const unsigned grid = (unsigned)(items_max < resident ? items_max : resident);
+    auto kern = a.conv_weight ? (a.decay_from_logit ? prep_kernel<true, true>
+                                                    : prep_kernel<true, false>)
+                              : (a.decay_from_logit ? prep_kernel<false, true>
+                                                    : prep_kernel<false, false>);
+    kern<<<grid, kPrepThreads, kPrepSmem, s>>>(t);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return e;

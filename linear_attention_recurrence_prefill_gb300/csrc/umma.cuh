@@ -270,6 +270,23 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Tiled tensor copy global -> shared through a tensor map (TMA), 3-D box at
+// coordinates (x, y, z) (x innermost, in elements; x * element size must be a
+// multiple of 16 bytes), completing its bytes on `bar`.  `tmap` is the generic
+// address of a CUtensorMap in kernel-parameter, constant or global memory.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const void* tmap, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(smem_u32(dst_smem)), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+// Fetch a tensor map's descriptor ahead of its first use.
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared; `src_bytes` < 16 zero-fills the
 // rest (0 = a zero chunk, nothing read).
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {

@@ -27,6 +27,14 @@ Workloads (all d_k = d_v = d):
                repeat every 64 tokens; q ~ N(0,1) unit-normalised, v ~ N(0,1),
                S0 = 0, gate as ``k3``; seed 4.
 
+The prologue from raw projections (``prologue_params``, ``conv_window``) draws
+synthetic parameters for the optional steps before the recurrence: short-
+convolution taps [3 (q, k, v), H, d, 4] ~ N(0, 0.5), decay logits ~ N(0, 1.5),
+per-head decay scales and per-channel decay biases either "wide" (A_h ~
+U[0.5, 2], b ~ N(0, 0.5)) or "workload" (A_h = 1, b = 0: the bounded sigmoid
+then gives the workloads' own log-alpha distribution -5 sigmoid(N(0, 1.5))),
+and windows of raw rows before each sequence ~ N(0, 1).
+
 "N(0, s)" is read as mean 0 and standard deviation s.  Draw order inside one
 workload: (lengths,) q, k, v, log-alpha noise, beta noise, gate noise, S0.
 Large tensors are drawn in token slabs so that the peak transient memory stays
@@ -189,6 +197,40 @@ def extreme(device="cpu", *, seed: int = 4, H: int = 96, T: int = 262144, d: int
     gate = _randn((T, H, d), g, device).to(dtype)
     return PrefillInputs(q, k, v, la, beta, None, gate, None, 1, 64, "extreme",
                          {"dtype": "bf16", "period": period})
+
+
+@dataclass
+class PrologueParams:
+    conv_weight: torch.Tensor   # [3, H, d, 4] fp32 (q, k, v taps, oldest row first)
+    decay_scale: torch.Tensor   # [H] fp32
+    decay_bias: torch.Tensor    # [H, d] fp32
+
+
+def prologue_params(device="cpu", *, H: int, d: int = 128, seed: int = 5,
+                    decay: str = "wide") -> PrologueParams:
+    """decay "wide": A_h ~ U[0.5, 2], b ~ N(0, 0.5) (exercises the scale and the
+    bias); "workload": A_h = 1, b = 0, which with logits ~ N(0, 1.5) gives the
+    workloads' own log-alpha distribution -5 sigmoid(N(0, 1.5))."""
+    g = _gen(seed, "cpu")
+    w = torch.randn((3, H, d, 4), generator=g) * 0.5
+    A = 0.5 + 1.5 * torch.rand((H,), generator=g)
+    b = torch.randn((H, d), generator=g) * 0.5
+    if decay == "workload":
+        A, b = torch.ones_like(A), torch.zeros_like(b)
+    elif decay != "wide":
+        raise ValueError(f"decay: 'wide' or 'workload', not {decay!r}")
+    return PrologueParams(w.to(device), A.to(device), b.to(device))
+
+
+def decay_logits(shape, device="cpu", *, seed: int = 6) -> torch.Tensor:
+    """Decay logits z ~ N(0, 1.5), fp32."""
+    return _randn(tuple(shape), _gen(seed, device), device, std=1.5)
+
+
+def conv_window(N: int, H: int, d: int = 128, device="cpu", *, seed: int = 7,
+                dtype=torch.bfloat16) -> torch.Tensor:
+    """Raw q, k, v rows of the 3 tokens before each sequence, [N, 3, 3, H, d]."""
+    return torch.randn((N, 3, 3, H, d), generator=_gen(seed, "cpu")).to(dtype).to(device)
 
 
 WORKLOADS = {

