@@ -43,7 +43,10 @@
 // ~16 significant bits, bf16 keeps the 2^+-116 range); every other product uses
 // fp16 operands (11 significant bits; all values there are within fp16 range
 // or negligibly small) with fp32 accumulation; the state itself stays fp32.
+#include <cuda.h>
 #include <stdio.h>
+
+#include <mutex>
 
 #include "kda_tc.cuh"
 #include "umma.cuh"
@@ -84,6 +87,11 @@ struct TcArgs {
   int total_chunks_max;   // upper bound of the chunk count (grid of prep)
   long long spins;        // bounded-wait limit
   int debug_timeout;
+  // Tensor maps of q, k, v as [T_total][H][128] bf16 (x = channel, y = head,
+  // z = token), box 64 channels x 1 head x 64 tokens, 128-byte swizzle: one box
+  // is half a chunk's rows of one head, landing as [64 rows][128 B] (the
+  // swizzled layout of sw128_chunk with 64 rows).  Tokens past T_total read 0.
+  CUtensorMap tm_q, tm_k, tm_v;
 };
 
 __device__ __forceinline__ void report(int* status, int code) { atomicExch(status, code); }
@@ -159,8 +167,9 @@ __device__ __forceinline__ int find_seq(const int* base, int N, int gid) {
 constexpr int kPrepThreads = 256;
 constexpr int kPrepHalf = 128;                   // threads per warp group (step 6)
 constexpr uint32_t kBarSolve = 2;                // the inverting group's named barrier
-constexpr uint32_t kPrepQ = 0;            // q rows, bf16 [64][128] (256 B rows)
-constexpr uint32_t kPrepK = 16384;        // k rows, bf16 [64][128]
+constexpr uint32_t kPrepQ = 0;            // q rows, bf16: two 64-channel halves of
+                                          // [64 rows][128 B], 128-byte swizzle (TMA)
+constexpr uint32_t kPrepK = 16384;        // k rows, the same
 constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
 constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
 //   Gram (per 64-channel half): B = [B_0; B_1] hi and lo, [96 x 64] bf16 K-major
@@ -231,10 +240,15 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
 // consecutive groups touch consecutive 16-byte words.
 __host__ __device__ constexpr int gpos(int ch) { return ((ch >> 2) & 1) * 64 + (ch >> 3) * 4 + (ch & 3); }
 
-// The input rows in shared memory (q, k: 16 chunks of 16 bytes; decay: 32) keep
-// chunk j of row r at chunk j ^ (r % 8), so that threads reading the same chunk
-// of eight consecutive rows hit eight different bank groups.
+// The decay rows in shared memory (32 chunks of 16 bytes) keep chunk j of row
+// r at chunk j ^ (r % 8), so that threads reading the same chunk of eight
+// consecutive rows hit eight different bank groups.  The q and k rows do the
+// same within each 128-byte half-row: the 16-byte chunk c16 (channels 8 c16 ..
+// 8 c16 + 7) of row r sits at qk_off(r, c16), the tensor copies' layout.
 __host__ __device__ constexpr int rsw(int r, int j) { return j ^ (r & 7); }
+__host__ __device__ __forceinline__ uint32_t qk_off(int r, int c16) {
+  return sw128_chunk((uint32_t)r, (uint32_t)c16, (uint32_t)kC);
+}
 // Float index in the decay rows of float f (as placed by gpos) of row r.
 __host__ __device__ constexpr int gsw(int r, int f) { return r * 128 + (rsw(r, f >> 2) << 2) + (f & 3); }
 
@@ -329,9 +343,9 @@ __device__ __forceinline__ void conv_taps4(const float* cw, int X, int H, int h,
 // formed from decay logits.  Separate instantiations, so that the default one
 // carries none of their registers.
 template <bool kConv, bool kLogit>
-__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_constant__ TcArgs t) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bar_mma;
+  __shared__ uint64_t bar_mma, bar_in, bar_v;  // MMAs; q/k tensor copies; v copies
   __shared__ uint32_t tmem_base;
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -345,9 +359,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   const int items = total * a.H;
   if ((int)blockIdx.x >= items) return;
   const size_t H = (size_t)a.H;
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
-  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
-  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
   const __nv_bfloat16* beta = static_cast<const __nv_bfloat16*>(a.beta);
   float* s_invq = reinterpret_cast<float*>(sm + kPrepSmall);
   float* s_invk = s_invq + 64;
@@ -356,7 +367,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 
   if (tid == 0) {
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_in, 1);
+    mbar_init(&bar_v, 1);
     mbar_fence_init();
+    tma_prefetch_desc(&t.tm_q);
+    tma_prefetch_desc(&t.tm_k);
+    tma_prefetch_desc(&t.tm_v);
   }
   if (warp == 0) {
     tmem_alloc(&tmem_base, kPrepTmemCols);
@@ -407,19 +423,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       }
       cp_async16(smem_u32(sm + kPrepHalo + (X * 3 + j) * 256 + c16 * 16), src, nbytes);
     }
-    // ---- 1. input rows by 16-byte asynchronous copies (all threads): q, k rows of
-    //      256 B and log alpha rows of 512 B; rows past the sequence end are
-    //      zero-filled (an identity step).  With one decay per head (or none) the
-    //      decay rows are filled by broadcasting the row's value instead ----
-    // q, k rows: 16-byte chunk e of row e / 16 (1024 chunks each)
-#pragma unroll 4
-    for (int e = tid; e < kC * 32; e += kPrepThreads) {
-      const int reg = e >> 10, wd = e & 1023, r = wd >> 4, col16 = wd & 15;
-      const int rr = r < len ? r : 0;
-      const char* src = reinterpret_cast<const char*>(reg ? (const void*)k : (const void*)q) +
-                        ((size_t)(tok0 + rr) * H + h) * 256 + (size_t)col16 * 16;
-      cp_async16(smem_u32(sm + (reg ? kPrepK : kPrepQ) + r * 256 + rsw(r, col16) * 16), src,
-                 r < len ? 16u : 0u);
+    // ---- 1. input rows: q and k by tensor copies (thread 0; two boxes each),
+    //      log alpha rows of 512 B by 16-byte asynchronous copies (all
+    //      threads).  q and k rows past the sequence end hold the next tokens (or
+    //      zeros past T_total): those rows are identity steps whatever their
+    //      values, since their beta and log alpha are 0.  With one decay per head
+    //      (or none) the decay rows are filled by broadcasting the row's value ----
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_in, 2 * kC * kD * 2);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        tma_load_3d(sm + kPrepQ + hf * 8192, &t.tm_q, 64 * hf, h, tok0, &bar_in);
+        tma_load_3d(sm + kPrepK + hf * 8192, &t.tm_k, 64 * hf, h, tok0, &bar_in);
+      }
     }
     if (a.decay_mode == KDA_DECAY_CHANNEL) {  // log alpha rows of 512 B
 #pragma unroll 4
@@ -448,13 +464,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
   int item = blockIdx.x, gid, h, tok0, len, nseq, sstart;
   decode(item, gid, h, tok0, len, nseq, sstart);
   issue_inputs(h, tok0, len, nseq, sstart);
-  uint32_t mma_phase = 0;
+  uint32_t mma_phase = 0, in_phase = 0, v_phase = 0;
+  bool in_pending = true, v_pending = false;  // tensor copies issued, not yet waited on
   bool ok = true;
   for (;;) {
     uint8_t* ws = ws_block(t, gid, h);
     cp_async_wait_all();
+    const bool in_ok = mbar_wait(&bar_in, in_phase, t.spins);
     if (tid == 0) bulk_wait_read();  // the previous item's results have left region X
-    __syncthreads();
+    ok = __syncthreads_and(in_ok);
+    if (!ok) goto fail;
+    in_phase ^= 1;
+    in_pending = false;
 
     // ---- 1b. short convolution + Swish of the q and k rows, in place: thread =
     //      (tensor, 8-row block rb, 8-channel group c16) streams its rows through
@@ -474,13 +495,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
           const int r = 8 * rb - 3 + j;
-          const uint8_t* src = r >= 0 ? rows + r * 256 + rsw(r, c16) * 16 : halo + (3 + r) * 256 + c16 * 16;
+          const uint8_t* src = r >= 0 ? rows + qk_off(r, c16) : halo + (3 + r) * 256 + c16 * 16;
           unpack4(*reinterpret_cast<const uint2*>(src + 8 * hf), win[j]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = 8 * rb + i;
-          uint2* p = reinterpret_cast<uint2*>(rows + r * 256 + rsw(r, c16) * 16 + 8 * hf);
+          uint2* p = reinterpret_cast<uint2*>(rows + qk_off(r, c16) + 8 * hf);
           const uint2 y = conv_row4(w, win, *p);
           if (i < 5) *p = y;
           else held[hf][i - 5] = y;
@@ -490,7 +511,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
 #pragma unroll
       for (int i = 5; i < 8; ++i) {
         const int r = 8 * rb + i;
-        *reinterpret_cast<uint4*>(rows + r * 256 + rsw(r, c16) * 16) =
+        *reinterpret_cast<uint4*>(rows + qk_off(r, c16)) =
             make_uint4(held[0][i - 5].x, held[0][i - 5].y, held[1][i - 5].x, held[1][i - 5].y);
       }
       __syncthreads();
@@ -532,13 +553,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       if (tid < kC) s_beta[tid] = (a.beta_is_logit && tid < len) ? sigmoidf_(bt) : bt;
     } else {
       // one row per thread (q rows 0..63, then k rows): its sixteen 16-byte chunks
-      // in an order rotated by the row, so that a warp's loads hit every bank
+      // (wherever the swizzle put them) in an order rotated by the row, so that a
+      // warp's loads hit every bank
       const int rr = tid - kD, r = rr & (kC - 1);
-      const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 256;
+      const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 128;
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint4 x = *reinterpret_cast<const uint4*>(src + (((i + rr) & 15) << 4));
+        const int p = (i + rr) & 15;  // physical chunk: half p / 8, position p % 8
+        const uint4 x = *reinterpret_cast<const uint4*>(src + (p >> 3) * 8192 + ((p & 7) << 4));
         const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -571,7 +594,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       // store is one for the whole warp: every lane takes the same group)
       const int rho = (warp & 3) * 32 + lane, r = rho & (kC - 1), khA = warp >> 2;
       const int mr = 32 * (r >> 5) + 15;
-      const uint8_t* xrow = sm + (rho < kC ? kPrepK : kPrepQ) + r * 256;
+      const uint8_t* xrows = sm + (rho < kC ? kPrepK : kPrepQ);
       const float inv = rho < kC ? s_invk[r] : s_invq[r];
       const float2 inv2 = make_float2(inv, inv);
 #pragma unroll 2
@@ -580,7 +603,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         float g8[8], m8[8], xf[8];
         ld8g(G, r, c, g8);
         ld8g(G, mr, c, m8);
-        unpack8(*reinterpret_cast<const uint4*>(xrow + rsw(r, c) * 16), xf);
+        unpack8(*reinterpret_cast<const uint4*>(xrows + qk_off(r, c)), xf);
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -610,8 +633,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
           const int j = ((tid + kPrepThreads * s3) - (s3 ? kPrepThreads : 0)) >> 3;
           float g8[8], kf[8];
           ld8g(G, j, 8 * kh + c8, g8);
-          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + j * 256 + rsw(j, 8 * kh + c8) * 16),
-                  kf);
+          unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + qk_off(j, 8 * kh + c8)), kf);
           const float ik = s_invk[j];
           const float2 ik2 = make_float2(ik, ik);
           uint32_t hi[4], lo[4];
@@ -686,8 +708,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       float g8[8], gl8[8], kf[8], qf[8];
       ld8g(G, r, c16, g8);
       ld8g(G, kC - 1, c16, gl8);
-      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + r * 256 + rsw(r, c16) * 16), kf);
-      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + r * 256 + rsw(r, c16) * 16), qf);
+      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + qk_off(r, c16)), kf);
+      unpack8(*reinterpret_cast<const uint4*>(sm + kPrepQ + qk_off(r, c16)), qf);
       const float ik = s_invk[r], iq = -s_invq[r];
       const float2 ik2 = make_float2(ik, ik), iq2 = make_float2(iq, iq);
       uint32_t wk[4], wq[4], wh[4];
@@ -716,16 +738,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
     if (!ok) goto fail;
     fence_after_sync();
     // every read of the q, k rows is done: they take K~ and the v rows (bf16, by
-    // 16-byte asynchronous copies that land during the solve), both MN-major
+    // two tensor copies that land during the solve), both MN-major (the q/k row
+    // layout is the MN-major operand layout)
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_v, kC * kD * 2);
+      tma_load_3d(sm + kPrepV, &t.tm_v, 0, h, tok0, &bar_v);
+      tma_load_3d(sm + kPrepV + 8192, &t.tm_v, 64, h, tok0, &bar_v);
+    }
+    v_pending = true;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int e = tid + kPrepThreads * m, r = e >> 4, c16 = e & 15;
       *reinterpret_cast<uint4*>(sm + kPrepKt + sw128_chunk(r, c16, kC)) = kt4[m];
-      const int rr = r < len ? r : 0;
-      cp_async16(smem_u32(sm + kPrepV + sw128_chunk(r, c16, kC)),
-                 v + ((size_t)(tok0 + rr) * H + h) * kD + 8 * c16, r < len ? 16u : 0u);
     }
-    cp_async_commit();
 
     {
       // ---- 4. A (lanes 0..63) to shared memory, P (lanes 64..127) to the workspace ----
@@ -908,11 +933,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
         *reinterpret_cast<uint4*>(sm + kPrepTlo + sw128_chunk(tr, c8, kC)) =
             make_uint4(tl[0], tl[1], tl[2], tl[3]);
       }
-      cp_async_wait_all();  // this thread's v rows have landed
+      // the v rows have landed once bar_v completes; the barrier that checks it
+      // is the one before the products (after the convolution's first barrier
+      // when the convolution is on)
+      const bool vok = mbar_wait(&bar_v, v_phase, t.spins);
       if constexpr (kConv) {
+        ok = __syncthreads_and(vok);
+        if (!ok) goto fail;
         // ---- 7b. short convolution + Swish of the v rows in place (MN-major
         //      tile): thread = (4-row block, 8-channel group) ----
-        __syncthreads();  // every thread's v rows have landed
         const int c16 = tid & 15, rb = tid >> 4;
         const uint8_t* halo = sm + kPrepHalo + 2 * 3 * 256;
         uint2 held[2][3];
@@ -943,7 +972,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       }
       fence_proxy_async();
       fence_before_sync();
-      __syncthreads();
+      ok = __syncthreads_and(vok);
+      if (!ok) goto fail;
+      v_phase ^= 1;
+      v_pending = false;
 
       // ---- 8. U~^T = V^T (T_hi + T_lo)^T (A = V MN-major bf16) and W = [T; T] K~
       //      (B = K~ MN-major fp16) on the tensor cores, then both straight to the
@@ -977,6 +1009,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(TcArgs t) {
       if (w_next < items) {
         decode(w_next, gid_n, h_n, tok0_n, len_n, n_n, s0_n);
         issue_inputs(h_n, tok0_n, len_n, n_n, s0_n);
+        in_pending = true;
       }
       {
         // U~^T and W go to the free region X in the workspace's byte layout (U~^T:
@@ -1039,6 +1072,8 @@ fail:
     report(a.status, KDA_ERR_TIMEOUT);
     mma_commit(&bar_mma);
     mbar_wait(&bar_mma, mma_phase, t.spins);
+    if (in_pending) mbar_wait(&bar_in, in_phase, t.spins);
+    if (v_pending) mbar_wait(&bar_v, v_phase, t.spins);
   }
 done:
   if (tid == 0) bulk_wait_all();
@@ -1424,6 +1459,41 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+// cuTensorMapEncodeTiled, reached through the runtime (no link against the
+// driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Tensor map of a [T][H][128] bf16 token array: box 64 channels x 1 head x 64
+// tokens, 128-byte swizzle (base 16-byte aligned, checked by the caller).
+bool encode_rows(CUtensorMap* m, const void* base, int T, int H) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (!fn || T < 1) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kC};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 size_t header_bytes(int N) { return ((size_t)(N + 1) * 4 + 1023) & ~(size_t)1023; }
 int chunks_upper(int T_total, int N) { return T_total / kC + N; }
 
@@ -1473,7 +1543,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
   chunk_base_kernel<<<1, 1024, 0, s>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return e;
-  if (t.total_chunks_max > 0 && !t.debug_timeout) {
+  if (a.T_total > 0 && t.total_chunks_max > 0 && !t.debug_timeout) {
+    if (!encode_rows(&t.tm_q, a.q, a.T_total, a.H) || !encode_rows(&t.tm_k, a.k, a.T_total, a.H) ||
+        !encode_rows(&t.tm_v, a.v, a.T_total, a.H))
+      return cudaErrorInvalidValue;
     // persistent: two CTAs per SM walk the (chunk, head) items
     const long long items_max = (long long)t.total_chunks_max * a.H;
     const long long resident = 2LL * (dev >= 0 && dev < 64 ? sm_count[dev] : 148);
