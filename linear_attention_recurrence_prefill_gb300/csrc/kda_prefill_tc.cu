@@ -90,8 +90,10 @@ struct TcArgs {
   // Tensor maps of q, k, v as [T_total][H][128] bf16 (x = channel, y = head,
   // z = token), box 64 channels x 1 head x 64 tokens, 128-byte swizzle: one box
   // is half a chunk's rows of one head, landing as [64 rows][128 B] (the
-  // swizzled layout of sw128_chunk with 64 rows).  Tokens past T_total read 0.
-  CUtensorMap tm_q, tm_k, tm_v;
+  // swizzled layout of sw128_chunk with 64 rows).  log alpha likewise as fp32
+  // (with one decay per key channel), box 32 channels x 1 x 64 tokens.  Tokens
+  // past T_total read 0.
+  CUtensorMap tm_q, tm_k, tm_v, tm_la;
 };
 
 __device__ __forceinline__ void report(int* status, int code) { atomicExch(status, code); }
@@ -170,7 +172,9 @@ constexpr uint32_t kBarSolve = 2;                // the inverting group's named 
 constexpr uint32_t kPrepQ = 0;            // q rows, bf16: two 64-channel halves of
                                           // [64 rows][128 B], 128-byte swizzle (TMA)
 constexpr uint32_t kPrepK = 16384;        // k rows, the same
-constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32 [64][128]
+constexpr uint32_t kPrepG = 32768;        // log alpha rows, then running log2-decay, fp32:
+                                          // four 32-channel slabs of [64 rows][128 B],
+                                          // 128-byte swizzle (TMA)
 constexpr uint32_t kPrepX = 65536;        // 40 KB region reused by the phases:
 //   Gram (per 64-channel half): B = [B_0; B_1] hi and lo, [96 x 64] bf16 K-major
 //   SW128 each (B_0: rows 0..31, B_1: rows 32..95)
@@ -234,30 +238,29 @@ __device__ __forceinline__ void unpack8(const uint4& r, float (&f)[8]) {
   }
 }
 
-// Decay rows in shared memory keep the two halves of each 8-channel group c in
-// separate 256-byte halves of the 512-byte row (channels 8c .. 8c+3 at float
-// 4c, channels 8c+4 .. 8c+7 at float 64 + 4c), so that threads reading
-// consecutive groups touch consecutive 16-byte words.
-__host__ __device__ constexpr int gpos(int ch) { return ((ch >> 2) & 1) * 64 + (ch >> 3) * 4 + (ch & 3); }
-
-// The decay rows in shared memory (32 chunks of 16 bytes) keep chunk j of row
-// r at chunk j ^ (r % 8), so that threads reading the same chunk of eight
-// consecutive rows hit eight different bank groups.  The q and k rows do the
-// same within each 128-byte half-row: the 16-byte chunk c16 (channels 8 c16 ..
-// 8 c16 + 7) of row r sits at qk_off(r, c16), the tensor copies' layout.
-__host__ __device__ constexpr int rsw(int r, int j) { return j ^ (r & 7); }
+// The q and k rows in shared memory keep, within each 128-byte half-row, the
+// 16-byte chunk c16 (channels 8 c16 .. 8 c16 + 7) of row r at qk_off(r, c16):
+// chunk j at position j ^ (r % 8), the tensor copies' 128-byte swizzle, so that
+// threads reading the same chunk of eight consecutive rows hit eight different
+// bank groups.
 __host__ __device__ __forceinline__ uint32_t qk_off(int r, int c16) {
   return sw128_chunk((uint32_t)r, (uint32_t)c16, (uint32_t)kC);
 }
-// Float index in the decay rows of float f (as placed by gpos) of row r.
-__host__ __device__ constexpr int gsw(int r, int f) { return r * 128 + (rsw(r, f >> 2) << 2) + (f & 3); }
+// The decay rows: four 32-channel slabs of [64 rows][128 B] with the same
+// swizzle.  Float index of channel ch of row r:
+__host__ __device__ constexpr int gidx(int r, int ch) {
+  return (ch >> 5) * 2048 + r * 32 + ((((ch >> 2) & 7) ^ (r & 7)) << 2) + (ch & 3);
+}
 
-// 8-channel group c of decay row r
+// 8-channel group c of decay row r: chunks 2 (c % 4) and 2 (c % 4) + 1 of slab
+// c / 4.  Odd slabs fetch the second chunk first, so that eight consecutive
+// groups of one row (two slabs) read eight different bank groups per load.
 __device__ __forceinline__ void ld8g(const float* G, int r, int c, float (&f)[8]) {
-  const float* row = G + r * 128;
-  const int p = rsw(r, c);
-  const float4 a = *reinterpret_cast<const float4*>(row + 4 * p);
-  const float4 b = *reinterpret_cast<const float4*>(row + 64 + 4 * p);
+  const float* row = G + (c >> 2) * 2048 + r * 32;
+  const int j = 2 * (c & 3), x = r & 7, odd = (c >> 2) & 1;
+  const float4 p = *reinterpret_cast<const float4*>(row + (((j + odd) ^ x) << 2));
+  const float4 q = *reinterpret_cast<const float4*>(row + (((j + 1 - odd) ^ x) << 2));
+  const float4 a = odd ? q : p, b = odd ? p : q;
   f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
@@ -373,6 +376,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     tma_prefetch_desc(&t.tm_q);
     tma_prefetch_desc(&t.tm_k);
     tma_prefetch_desc(&t.tm_v);
+    if (a.decay_mode == KDA_DECAY_CHANNEL) tma_prefetch_desc(&t.tm_la);
   }
   if (warp == 0) {
     tmem_alloc(&tmem_base, kPrepTmemCols);
@@ -423,40 +427,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       }
       cp_async16(smem_u32(sm + kPrepHalo + (X * 3 + j) * 256 + c16 * 16), src, nbytes);
     }
-    // ---- 1. input rows: q and k by tensor copies (thread 0; two boxes each),
-    //      log alpha rows of 512 B by 16-byte asynchronous copies (all
-    //      threads).  q and k rows past the sequence end hold the next tokens (or
-    //      zeros past T_total): those rows are identity steps whatever their
-    //      values, since their beta and log alpha are 0.  With one decay per head
-    //      (or none) the decay rows are filled by broadcasting the row's value ----
+    // ---- 1. input rows by tensor copies (thread 0): q and k (two boxes each)
+    //      and, with one decay per key channel, log alpha (four boxes).  Rows
+    //      past the sequence end hold the next tokens (or zeros past T_total):
+    //      they are identity steps whatever their q, k, v, since their beta is 0
+    //      and the decay scan takes their log alpha as 0.  With one decay per
+    //      head (or none) the decay rows are filled by broadcasting the row's
+    //      value instead ----
+    const bool la_tma = a.decay_mode == KDA_DECAY_CHANNEL;
     if (tid == 0) {
-      mbar_arrive_expect_tx(&bar_in, 2 * kC * kD * 2);
+      mbar_arrive_expect_tx(&bar_in, 2 * kC * kD * 2 + (la_tma ? kC * kD * 4 : 0));
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         tma_load_3d(sm + kPrepQ + hf * 8192, &t.tm_q, 64 * hf, h, tok0, &bar_in);
         tma_load_3d(sm + kPrepK + hf * 8192, &t.tm_k, 64 * hf, h, tok0, &bar_in);
       }
-    }
-    if (a.decay_mode == KDA_DECAY_CHANNEL) {  // log alpha rows of 512 B
-#pragma unroll 4
-      for (int e = tid; e < kC * 32; e += kPrepThreads) {
-        const int r = e >> 5, col16 = e & 31;
-        const int rr = r < len ? r : 0;
-        const char* src = reinterpret_cast<const char*>(a.log_alpha) +
-                          ((size_t)(tok0 + rr) * H + h) * 512 + (size_t)col16 * 16;
-        // channels 4 col16 .. +3: group col16 / 2, half col16 % 2
-        cp_async16(smem_u32(sm + kPrepG + r * 512 + (col16 & 1) * 256 + rsw(r, col16 >> 1) * 16),
-                   src,
-                   r < len ? 16u : 0u);
+      if (la_tma) {
+#pragma unroll
+        for (int sl = 0; sl < 4; ++sl)
+          tma_load_3d(sm + kPrepG + sl * 8192, &t.tm_la, 32 * sl, h, tok0, &bar_in);
       }
     }
     cp_async_commit();
-    if (a.decay_mode != KDA_DECAY_CHANNEL) {
+    if (!la_tma) {
       for (int e = tid; e < kC * 32; e += kPrepThreads) {  // 16-byte words of the rows
         const int r = e >> 5, wd = e & 31;
         const float g = (r < len && a.decay_mode == KDA_DECAY_HEAD)
                             ? a.log_alpha[(size_t)(tok0 + r) * H + h] : 0.f;
-        *reinterpret_cast<float4*>(sm + kPrepG + r * 512 + wd * 16) = make_float4(g, g, g, g);
+        *reinterpret_cast<float4*>(sm + kPrepG + (wd >> 3) * 8192 + r * 128 + (wd & 7) * 16) =
+            make_float4(g, g, g, g);
       }
     }
   };
@@ -519,20 +518,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
     //      registers); L2 norms of the q, k rows (warps 4-7, one row per thread) ----
-    if (tid < kD) {  // thread tid scans float tid (as placed by gpos) of the rows
+    if (tid < kD) {  // thread tid scans channel tid of the rows
       // beta of row tid: loaded here, stored after the scan, so that the scan hides
       // its latency
       float bt = 0.f;
       if (tid < len) bt = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
       float dA = 1.f, db = 0.f;  // decay from logits: scale and this channel's bias
       if constexpr (kLogit) {
-        const int ch = ((tid & 63) >> 2) * 8 + (tid >> 6) * 4 + (tid & 3);  // gpos^-1
         if (a.decay_scale) dA = a.decay_scale[h];
-        if (a.decay_bias) db = a.decay_bias[(size_t)h * kD + ch];
+        if (a.decay_bias) db = a.decay_bias[(size_t)h * kD + tid];
       }
       float x[kC];
 #pragma unroll
-      for (int r = 0; r < kC; ++r) x[r] = G[gsw(r, tid)];
+      for (int r = 0; r < kC; ++r) x[r] = G[gidx(r, tid)];
       float run = 0.f;
       if constexpr (kLogit) {  // log alpha = g_min sigmoid(A (z + b)); rows past
 #pragma unroll                   // the sequence end stay at 0 (identity steps)
@@ -541,15 +539,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
           run += fminf(fmaxf(la, a.g_min), 0.f) * kLog2e;
           x[r] = run;
         }
-      } else {
+      } else {  // rows past the sequence end: log alpha 0
 #pragma unroll
         for (int r = 0; r < kC; ++r) {
-          run += fminf(fmaxf(x[r], a.g_min), 0.f) * kLog2e;
+          run += (r < len ? fminf(fmaxf(x[r], a.g_min), 0.f) : 0.f) * kLog2e;
           x[r] = run;
         }
       }
 #pragma unroll
-      for (int r = 0; r < kC; ++r) G[gsw(r, tid)] = x[r];
+      for (int r = 0; r < kC; ++r) G[gidx(r, tid)] = x[r];
       if (tid < kC) s_beta[tid] = (a.beta_is_logit && tid < len) ? sigmoidf_(bt) : bt;
     } else {
       // one row per thread (q rows 0..63, then k rows): its sixteen 16-byte chunks
@@ -732,7 +730,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       *reinterpret_cast<uint4*>(ws + kWsKh + sw128_chunk(r, c16, kC)) =
           make_uint4(wh[0], wh[1], wh[2], wh[3]);
     }
-    if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(G[gsw(kC - 1, gpos(tid))]);
+    if (tid < kD) reinterpret_cast<float*>(ws + kWsGam)[tid] = ex2f(G[gidx(kC - 1, tid)]);
     ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
     mma_phase ^= 1;
     if (!ok) goto fail;
@@ -1479,19 +1477,21 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// Tensor map of a [T][H][128] bf16 token array: box 64 channels x 1 head x 64
-// tokens, 128-byte swizzle (base 16-byte aligned, checked by the caller).
-bool encode_rows(CUtensorMap* m, const void* base, int T, int H) {
+// Tensor map of a [T][H][128] token array of 2-byte (bf16) or 4-byte (fp32)
+// elements: box 128 bytes of channels x 1 head x 64 tokens, 128-byte swizzle
+// (base 16-byte aligned, checked by the caller).
+bool encode_rows(CUtensorMap* m, const void* base, int T, int H, bool fp32) {
   const EncodeTiledFn fn = encode_tiled();
   if (!fn || T < 1) return false;
+  const cuuint64_t esize = fp32 ? 4 : 2;
   const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
-  const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kC};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * esize, (cuuint64_t)H * kD * esize};
+  const cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)kC};
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 size_t header_bytes(int N) { return ((size_t)(N + 1) * 4 + 1023) & ~(size_t)1023; }
@@ -1544,8 +1544,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return e;
   if (a.T_total > 0 && t.total_chunks_max > 0 && !t.debug_timeout) {
-    if (!encode_rows(&t.tm_q, a.q, a.T_total, a.H) || !encode_rows(&t.tm_k, a.k, a.T_total, a.H) ||
-        !encode_rows(&t.tm_v, a.v, a.T_total, a.H))
+    if (!encode_rows(&t.tm_q, a.q, a.T_total, a.H, false) ||
+        !encode_rows(&t.tm_k, a.k, a.T_total, a.H, false) ||
+        !encode_rows(&t.tm_v, a.v, a.T_total, a.H, false) ||
+        (a.decay_mode == KDA_DECAY_CHANNEL &&
+         !encode_rows(&t.tm_la, a.log_alpha, a.T_total, a.H, true)))
       return cudaErrorInvalidValue;
     // persistent: two CTAs per SM walk the (chunk, head) items
     const long long items_max = (long long)t.total_chunks_max * a.H;
