@@ -183,7 +183,10 @@ size_t kda_prefill_workspace_size(int T_total, int N, int H, int d_k, int d_v,
  * The implementation kda_prefill runs for these sizes and options: returns
  * KDA_IMPL_SIMT or KDA_IMPL_TC (> 0), or a negative status if kda_prefill
  * would reject them.  *launches (if not NULL) receives the number of kernels
- * one call enqueues, *chunk (if not NULL) the chunk length it uses.
+ * one call enqueues with cu_seqlens (the tensor-core path enqueues one fewer
+ * for equal-length sequences, cu_seqlens NULL: it needs no chunk-base prefix
+ * sum, and the first phase_events interval is then empty), *chunk (if not
+ * NULL) the chunk length it uses.
  */
 int kda_prefill_path(int T_total, int N, int H, int d_k, int d_v, int dtype,
                      const kda_options* opt, int* launches, int* chunk);

@@ -358,7 +358,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
   // ---- work items: (chunk, head) pairs, item w = h * total + gid; a CTA takes
   //      items blockIdx.x, + gridDim.x, ... and streams the next item's inputs
   //      into its buffers while it writes out the current one ----
-  const int total = t.chunk_base[a.N];
+  // the chain may start its CTAs (set-up only) as SMs free up at this grid's end
+  grid_launch_dependents();
+  // sequences of one length L (no cu_seqlens) have ceil(L / C) chunks each: the
+  // item's tokens follow by arithmetic, without a dependent load
+  const int L_eq = a.cu_seqlens ? 0 : a.T_total / a.N;
+  const int cps_eq = (L_eq + kC - 1) / kC;
+  const int total = a.cu_seqlens ? t.chunk_base[a.N] : a.N * cps_eq;
   const int items = total * a.H;
   if ((int)blockIdx.x >= items) return;
   const size_t H = (size_t)a.H;
@@ -387,10 +393,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
   fence_after_sync();
   const uint32_t tmem = tmem_base;
 
-  // sequences of one length L (no cu_seqlens) have ceil(L / C) chunks each: the
-  // item's tokens follow by arithmetic, without a dependent load
-  const int L_eq = a.cu_seqlens ? 0 : a.T_total / a.N;
-  const int cps_eq = (L_eq + kC - 1) / kC;
   auto decode = [&](int wi, int& gid_, int& h_, int& tok0_, int& len_, int& n_, int& s0_) {
     h_ = wi / total;
     gid_ = wi - h_ * total;
@@ -1136,7 +1138,9 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   seq_range(a.cu_seqlens, a.N, a.T_total, n, s0, s1);
   if (s0 < 0 || s1 < s0 || s1 > a.T_total) return;  // reported by chunk_base_kernel
   const int nchunks = (s1 - s0 + kC - 1) / kC;
-  const int cbase = t.chunk_base[n];
+  // first chunk of the sequence (equal lengths: by arithmetic; the chunk bases
+  // are complete before the prep grid starts)
+  const int cbase = a.cu_seqlens ? t.chunk_base[n] : n * nchunks;
   const size_t sbase = ((size_t)n * H + h) * (size_t)(kD * kD);
 
   if (tid == 0) {
@@ -1170,6 +1174,9 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   };
   int issued = 0;  // loads issued (kLoader)
   if (tid == kLoader) {
+    // the chunk blocks are the prep grid's output: everything above overlaps its
+    // end when this grid starts early
+    grid_wait_prerequisites();
     for (int i = 0; i < 2 && i < nchunks; ++i) issue_load(i);
     issued = min(2, nchunks);
   }
@@ -1540,9 +1547,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
     attr_done[dev] = true;
   }
   if (ev && (e = cudaEventRecord(ev[0], s)) != cudaSuccess) return e;
-  chunk_base_kernel<<<1, 1024, 0, s>>>(t);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.cu_seqlens) {  // equal lengths need no chunk bases (their interval stays empty)
+    chunk_base_kernel<<<1, 1024, 0, s>>>(t);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   if (ev && (e = cudaEventRecord(ev[1], s)) != cudaSuccess) return e;
+  bool prep_launched = false;
   if (a.T_total > 0 && t.total_chunks_max > 0 && !t.debug_timeout) {
     if (!encode_rows(&t.tm_q, a.q, a.T_total, a.H, false) ||
         !encode_rows(&t.tm_k, a.k, a.T_total, a.H, false) ||
@@ -1560,10 +1570,24 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, const kda_options* opt, cuda
                                                     : prep_kernel<false, false>);
     kern<<<grid, kPrepThreads, kPrepSmem, s>>>(t);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    prep_launched = true;
   }
   if (ev && (e = cudaEventRecord(ev[2], s)) != cudaSuccess) return e;
-  chain_kernel<<<(unsigned)(a.N * a.H), kChThreads, kChSmem, s>>>(t);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // After prep the chain starts early (programmatic dependent launch): its CTAs
+  // load S0 and the first gate rows while prep's last items finish, and wait for
+  // prep before reading its blocks.  Without prep it launches in order: it reads
+  // S0 before that wait, which the kernels before it may have written.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.N * a.H));
+  cfg.blockDim = dim3(kChThreads);
+  cfg.dynamicSmemBytes = kChSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = prep_launched ? 1 : 0;
+  if ((e = cudaLaunchKernelEx(&cfg, chain_kernel, t)) != cudaSuccess) return e;
   if (ev && (e = cudaEventRecord(ev[3], s)) != cudaSuccess) return e;
   return cudaSuccess;
 }

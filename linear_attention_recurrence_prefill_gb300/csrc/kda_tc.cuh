@@ -12,7 +12,8 @@ bool tc_prefill_supported(int d, int dtype, int chunk);
 // Workspace bytes the tensor-core path needs for these sizes.
 size_t tc_workspace_bytes(int T_total, int N, int H, int d, const kda_options* opt);
 
-// Kernels one tensor-core prefill call enqueues, and its chunk length.
+// Kernels one tensor-core prefill call enqueues (with cu_seqlens; a call of
+// equal-length sequences skips the first, the chunk bases), and its chunk length.
 int tc_launches(int T_total, int N, int H, int d, const kda_options* opt);
 int tc_chunk(const kda_options* opt);
 
