@@ -19,7 +19,9 @@ namespace {
 
 constexpr int kDecThreads = 256;
 
-template <int D, typename T>
+// kConv: the short convolution runs on the token's q, k, v first (a separate
+// instantiation, so that the default one carries none of its registers).
+template <int D, typename T, bool kConv>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
   constexpr int C4 = D / 4;               // float4 per state row
   constexpr int RPP = kDecThreads / C4;   // rows per pass
@@ -56,7 +58,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
     kv = to_f32(k[base + tid]);
     vv = to_f32(v[base + tid]);
     lav = log_alpha_at(a.log_alpha, a.decay_mode, (size_t)unit, D, tid);
-    if (a.conv_weight) {
+    if constexpr (kConv) {
 #pragma unroll
       for (int X = 0; X < 3; ++X) {
         cw[X] = *reinterpret_cast<const float4*>(a.conv_weight +
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(DecodeArgs a) {
   }
   if (tid == 0) bv = to_f32(static_cast<const T*>(a.beta)[unit]);
   if (tid < D) {
-    if (a.conv_weight) {  // conv over (3 previous rows, this row), then Swish,
+    if constexpr (kConv) {  // conv over (3 previous rows, this row), then Swish,
       const float raw[3] = {qv, kv, vv};  // held in the data type
       float y[3];
 #pragma unroll
@@ -209,7 +211,8 @@ __global__ void gated_rmsnorm_kernel(const T* o, const T* __restrict__ gate,
 template <int D, typename T>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   const unsigned grid = (unsigned)a.N * (unsigned)a.H;
-  decode_kernel<D, T><<<grid, kDecThreads, 0, s>>>(a);
+  if (a.conv_weight) decode_kernel<D, T, true><<<grid, kDecThreads, 0, s>>>(a);
+  else decode_kernel<D, T, false><<<grid, kDecThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -253,8 +253,19 @@ __host__ __device__ constexpr int gidx(int r, int ch) {
 }
 
 // 8-channel group c of decay row r: chunks 2 (c % 4) and 2 (c % 4) + 1 of slab
-// c / 4.  Odd slabs fetch the second chunk first, so that eight consecutive
-// groups of one row (two slabs) read eight different bank groups per load.
+// c / 4, for accesses where the lanes of a warp read the same group of
+// different rows (the row's swizzle keeps those conflict-free).
+__device__ __forceinline__ void ld8g_rows(const float* G, int r, int c, float (&f)[8]) {
+  const float* row = G + (c >> 2) * 2048 + r * 32;
+  const int j = 2 * (c & 3), x = r & 7;
+  const float4 a = *reinterpret_cast<const float4*>(row + ((j ^ x) << 2));
+  const float4 b = *reinterpret_cast<const float4*>(row + (((j + 1) ^ x) << 2));
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+// The same where the lanes read consecutive groups of one row: odd slabs fetch
+// the second chunk first, so that eight consecutive groups (two slabs) read
+// eight different bank groups per load.
 __device__ __forceinline__ void ld8g(const float* G, int r, int c, float (&f)[8]) {
   const float* row = G + (c >> 2) * 2048 + r * 32;
   const int j = 2 * (c & 3), x = r & 7, odd = (c >> 2) & 1;
@@ -601,8 +612,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       for (int gi = 0; gi < 8; ++gi) {
         const int c = 8 * khA + gi;
         float g8[8], m8[8], xf[8];
-        ld8g(G, r, c, g8);
-        ld8g(G, mr, c, m8);
+        ld8g_rows(G, r, c, g8);
+        ld8g_rows(G, mr, c, m8);
         unpack8(*reinterpret_cast<const uint4*>(xrows + qk_off(r, c)), xf);
         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -619,20 +630,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       }
     }
     {
-      // B items of half kh: e = tid + 256 s3 -- span 0 rows for s3 = 0, span 1
-      // rows for s3 = 1, 2 -- each one row j and the 8-channel group tid % 8
-      const int c8 = tid & 7;
+      // B items of half kh: warp w takes the 8-channel group w of the half, lane
+      // l the B rows 32 s3 + l (s3 = 0: span 0 row l; s3 = 1, 2: span 1 row
+      // 32 (s3 - 1) + l), so that a warp reads one group of 32 rows
+      const int c8 = warp;
       uint4 vh[3], vl[3];
       uint32_t vo[3];
       auto b_items = [&](int kh) {
         float m0[8], m1[8];
-        ld8g(G, 15, 8 * kh + c8, m0);
-        ld8g(G, 47, 8 * kh + c8, m1);
+        ld8g_rows(G, 15, 8 * kh + c8, m0);  // the same for every lane
+        ld8g_rows(G, 47, 8 * kh + c8, m1);
 #pragma unroll
         for (int s3 = 0; s3 < 3; ++s3) {
-          const int j = ((tid + kPrepThreads * s3) - (s3 ? kPrepThreads : 0)) >> 3;
+          const int j = s3 == 0 ? lane : 32 * (s3 - 1) + lane;
           float g8[8], kf[8];
-          ld8g(G, j, 8 * kh + c8, g8);
+          ld8g_rows(G, j, 8 * kh + c8, g8);
           unpack8(*reinterpret_cast<const uint4*>(sm + kPrepK + qk_off(j, 8 * kh + c8)), kf);
           const float ik = s_invk[j];
           const float2 ik2 = make_float2(ik, ik);
@@ -647,7 +659,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
           }
           vh[s3] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           vl[s3] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          vo[s3] = sw128_chunk((s3 ? 32 : 0) + j, c8, 96);
+          vo[s3] = sw128_chunk(32 * s3 + lane, c8, 96);
         }
       };
       auto b_store = [&]() {
