@@ -78,3 +78,32 @@ def test_noalloc_refuses_sizes_beyond_the_scratch():
     assert not o.any() and not S_T.any()          # nothing was launched
     with pytest.raises(kda.KdaError):
         kda.kda_prefill_noalloc(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.S0)
+
+
+def test_noalloc_at_the_size_limit():
+    """The largest size whose scratch fits the array runs (and equals
+    kda_prefill bit for bit); one chunk more is refused before anything runs."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda")
+    H = 8
+    # scratch = header + H * (T / 64 + N) blocks: the largest T (a multiple of 64)
+    # that fits, and the next one
+    T = 64
+    while kda.kda_prefill_workspace_size(T + 64, 1, H, 128, 128) <= kda.NOALLOC_SCRATCH_BYTES:
+        T += 64
+    assert kda.kda_prefill_workspace_size(T, 1, H, 128, 128) <= kda.NOALLOC_SCRATCH_BYTES
+    inp = inputs.k3(dev, H=H, T=T, seed=33)
+    o = torch.empty_like(inp.q)
+    S_T = torch.empty((1, H, 128, 128), dtype=torch.float32, device=dev)
+    assert _noalloc_c(inp, o, S_T) == kda.KDA_OK
+    torch.cuda.synchronize()
+    assert kda.kda_get_last_error() == kda.KDA_OK
+    o_ref, S_ref = _reference(inp)
+    assert torch.equal(o, o_ref) and torch.equal(S_T, S_ref)
+    big = inputs.k3(dev, H=H, T=T + 64, seed=34)
+    o2 = torch.zeros_like(big.q)
+    S2 = torch.zeros((1, H, 128, 128), dtype=torch.float32, device=dev)
+    assert _noalloc_c(big, o2, S2) == kda.KDA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert not o2.any() and not S2.any()
