@@ -109,6 +109,22 @@ def test_varlen_small_edges():
 
 
 @pytest.mark.parametrize("impl", IMPLS)
+def test_many_short_sequences(impl):
+    """2,500 packed sequences of 0..12 tokens (many empty, none a full chunk):
+    the chunk-base prefix sum runs over several blocks of sequences and each
+    chunk finds its sequence by search; every sequence starts from its own
+    state."""
+    dev = _cuda()
+    g = torch.Generator().manual_seed(47)
+    lens = torch.randint(0, 13, (2500,), generator=g).tolist()
+    inp = inputs.varlen(dev, H=2, lengths=lens)
+    inp.S0 = torch.randn((len(lens), 2, 128, 128), device=dev) * 0.05
+    o, S_T = _check(inp, impl, TOL_BF16, max_seqlen=max(lens))
+    empty = [n for n, L in enumerate(lens) if L == 0]
+    assert empty and torch.equal(S_T[empty], inp.S0[empty])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 def test_varlen_equals_separate_calls(impl):
     """Packed sequences give exactly what separate calls on each one give: every
     chunk restarts at its sequence start, and the kernels do the same arithmetic
