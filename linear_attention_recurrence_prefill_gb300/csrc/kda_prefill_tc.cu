@@ -9,17 +9,24 @@
 // every block of the chunk, the diagonal ones included, is a dense tensor-core
 // product.  Three kernels per call:
 //
-//   1. chunk_base_kernel   prefix sum of chunks per sequence (varlen support).
+//   1. chunk_base_kernel   prefix sum of chunks per sequence (varlen support;
+//                          not launched for sequences of one length, whose
+//                          chunks follow by arithmetic).
 //   2. prep_kernel         persistent, two CTAs per SM walking the (chunk, head)
-//                          items, all independent; per item: prologue (L2 norm, beta, log-decay floor and running
-//                          sum), the decay-rescaled Gram matrices A and P on the
+//                          items, all independent; the inputs of each item
+//                          arrive by TMA tensor copies; per item: prologue
+//                          (optionally the short convolution and the decay from
+//                          its logit, then L2 norm, beta, log-decay floor and
+//                          running sum), the decay-rescaled Gram matrices A and P on the
 //                          tensor cores (bf16 hi/lo split, three products, fp32
 //                          accumulation in TMEM), the unit-lower-triangular solve
 //                          T = (I + A)^-1 Diag(beta) in fp32, then W = T K~ and
 //                          U~ = T V on the tensor cores.  Writes one 72.5 KB
 //                          block per (chunk, head) to the workspace, already in
 //                          the shared-memory operand layout of kernel 3.
-//   3. chain_kernel        one CTA per (sequence, head), walking the chunks in
+//   3. chain_kernel        one CTA per (sequence, head), launched early
+//                          (programmatic dependent launch) so that its set-up
+//                          overlaps prep's last items, walking the chunks in
 //                          order with the state S^T resident in TMEM (fp32):
 //                            U^T  = U~^T - S^T W^T
 //                            O^T  = S^T Q~^T + U^T P^T
