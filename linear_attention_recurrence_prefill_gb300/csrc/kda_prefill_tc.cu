@@ -198,13 +198,22 @@ constexpr uint32_t kPrepTT = kPrepX, kPrepV = kPrepQ, kPrepKt = kPrepK;
 constexpr uint32_t kPrepThi = kPrepG, kPrepTlo = kPrepG + 8192;
 //   U~^T and W staged for their bulk copies to the workspace
 constexpr uint32_t kPrepStU = kPrepX, kPrepStW = kPrepX + 16384;
-//   Z = A_10 X_00 of the inverse (fp32 [32][32]) over the decay rows, which the
-//   row pass has finished reading and the T tiles take only later
-constexpr uint32_t kPrepZ = kPrepG;
+//   the inverse's 32-level products: B operands A_10^T and -X_00^T as bf16 hi/lo
+//   K-major tiles [32 (column) rows][K = 32 in the first 64 B of each 128-byte
+//   row], SW128, over the decay rows behind the T tiles (the row pass has
+//   finished reading them)
+constexpr uint32_t kPrepA10h = kPrepG + 16384, kPrepA10l = kPrepA10h + 4096;
+constexpr uint32_t kPrepX00h = kPrepA10h + 8192, kPrepX00l = kPrepA10h + 12288;
 // TMEM: the Gram's D = [D_0 | D_1] (32 + 64 columns) and A (hi, lo for each
 // channel half: 4 x 32); then U~^T (64 columns) and W (128)
 constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
 constexpr uint32_t kTdU = 0, kTdW = 64;
+// the inverse (between the two): lanes 0..31 carry rows 32..63; A = X_11 as
+// bf16 hi/lo (16 + 16 columns), D = X_11 A_10, A = that product as hi/lo, and
+// D = X_10
+constexpr uint32_t kTdX11 = 128, kTdY = 160, kTdYs = 192, kTdX10 = 224;
+static_assert(kTdX10 + 32 <= kPrepTmemCols, "the inverse's operands fit the TMEM allocation");
+constexpr uint32_t kIdInv = idesc_f16(128, 32, true);  // bf16, N = 32
 static_assert(kTdA + 128 <= kPrepTmemCols, "Gram accumulators and A fit the TMEM allocation");
 static_assert(kTdW + 128 <= kPrepTmemCols, "W fits the TMEM allocation");
 constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
@@ -218,6 +227,8 @@ static_assert(kPrepY + 4 * 256 * 4 <= kPrepSmall, "solve scratch inside the reus
 static_assert(kPrepBl + 12288 <= kPrepSmall, "Gram operands inside the reused region");
 static_assert(kPrepTT + 2 * kC * 128 <= kPrepInv, "[T; T] tile clear of the inverse");
 static_assert(kPrepStW + 16384 <= kPrepSmall, "U~^T and W staging inside the reused region");
+static_assert(kPrepTlo + 8192 <= kPrepA10h && kPrepX00l + 4096 <= kPrepX,
+              "the inverse's operand tiles clear of the T tiles, inside the decay rows");
 static_assert(kPrepInv % 16 == 0 && kPrepY % 16 == 0 && (kXs * 4) % 16 == 0,
               "float4 access to the inverse and the scratch");
 
@@ -814,13 +825,28 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       fence_before_sync();
       __syncthreads();
 
-      // ---- 6. X = (I + A)^-1 in fp32: warps 0-1 invert the diagonal 16-blocks
-      //      while warps 4-7 clear the blocks above the diagonal; then warps 0-3
-      //      complete the diagonal 32-blocks (named barriers) while warps 4-7 form
-      //      the parts of Z = A_10 X_00 that need only the diagonal 16-blocks ----
+      // ---- 6. X = (I + A)^-1: warps 0-1 invert the diagonal 16-blocks (fp32)
+      //      while warps 4-7 clear the blocks above the diagonal and lay out the
+      //      B operand A_10^T; warps 0-3 then complete the diagonal 32-blocks
+      //      (fp32, named barrier), and warp 0 forms the lower 32-block
+      //      X_10 = -X_11 A_10 X_00 = (X_11 A_10) (-X_00) by two bf16 hi/lo
+      //      products on the tensor cores (as the Gram), while the other warps
+      //      write T's first 32 rows ----
       float* X = reinterpret_cast<float*>(sm + kPrepInv);
       float* Y = reinterpret_cast<float*>(sm + kPrepY);
-      float* Z = reinterpret_cast<float*>(sm + kPrepZ);
+      // K-major bf16 hi/lo tile of the B operand tile[c][m] = sgn * src[m][c]
+      // (m, c = 0..31; src row stride ld): 8 rows m of column c per unit
+      auto b_tile = [&](const float* src, int ld, float sgn, uint32_t thi, uint32_t tlo,
+                        int c, int m8) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          split2v(make_float2(sgn * src[(8 * m8 + 2 * u) * ld + c],
+                              sgn * src[(8 * m8 + 2 * u + 1) * ld + c]), hi[u], lo[u]);
+        const uint32_t o = sw128_chunk(c, m8, 32);
+        *reinterpret_cast<uint4*>(sm + thi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sm + tlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      };
       if (tid >= kPrepHalf) {
         for (int e = tid - kPrepHalf; e < 6 * 256; e += kPrepHalf) {
           const int blk = e >> 8, r = (e >> 4) & 15, cc = e & 15;
@@ -828,6 +854,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
           const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
           X[(16 * bi + r) * kXs + 16 * bj + cc] = 0.f;
         }
+        // A_10 = A rows 32..63, columns 0..31; unit (column c = lane, 8 rows m8)
+        const int u = tid - kPrepHalf;
+        b_tile(Amat + 32 * kAs, kAs, 1.f, kPrepA10h, kPrepA10l, u & 31, u >> 5);
+        fence_proxy_async();
       } else if (tid < 64) {  // diagonal blocks: thread = (block bi, column cc); right-looking
           const int bi = tid >> 4, cc = tid & 15, o = 16 * bi;  // (x[m] final -> update
           float x[16];                                          // rows below: 15-FMA chain)
@@ -842,28 +872,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
           for (int r = 0; r < 16; ++r) X[(o + r) * kXs + o + cc] = x[r];
       }
       __syncthreads();  // the diagonal 16-blocks are complete, the upper blocks clear
-      if (tid >= kPrepHalf) {
-        // Z = A_10 X_00 (A_10: A rows 32..63, columns 0..31) without its x10 term:
-        // columns 16..31 in full (A_10[:, 16..31] x11), columns 0..15 as far as
-        // A_10[:, 0..15] x00.  Unit = (row r, 4 columns c4), two per thread.
-        for (int e = tid - kPrepHalf; e < 32 * 8; e += kPrepHalf) {
-          const int r = e >> 3, c4 = (e & 7) * 4, b = c4 >> 4;
-          const float2* arow = reinterpret_cast<const float2*>(Amat + (32 + r) * kAs + 16 * b);
-          const float* xb = X + 16 * b * kXs + c4;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int m2 = 0; m2 < 8; ++m2) {
-            const float2 am = arow[m2];
-            fma4s(acc, am.x, *reinterpret_cast<const float4*>(xb + 2 * m2 * kXs));
-            fma4s(acc, am.y, *reinterpret_cast<const float4*>(xb + (2 * m2 + 1) * kXs));
-          }
-          *reinterpret_cast<float4*>(Z + r * 32 + c4) = acc;
-        }
-      } else {
+      if (tid < kPrepHalf) {
         // 2 x 2 block inverse at 32 x 32: the lower 16 x 16 block of each diagonal
-        // 32-block, X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (B1, B2);
-        // the lower 32-block follows below with all threads (C1, C2).  Each unit
-        // is 4 adjacent columns of one row (float4 loads), unrolled.
+        // 32-block, X_{2p+1,2p} = -X_{2p+1,2p+1} A_{2p+1,2p} X_{2p,2p} (B1, B2).
+        // Each unit is 4 adjacent columns of one row (float4 loads), unrolled.
         {  // B1: Y_p = A_{2p+1,2p} X_{2p,2p}; unit (p, r, c4)
           const int p = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
           const int i1 = 16 * (2 * p + 1), i0 = 32 * p;
@@ -897,43 +909,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         }
       }
       __syncthreads();  // the diagonal 32-blocks of X are complete
-      // the lower 32-block, X_10 = -X_11 A_10 X_00: unit = (row r, 4 columns c4)
-      if (tid < kPrepHalf) {  // Z[:, 0..15] += A_10[:, 16..31] x10 (the same order of
-        const int r = tid >> 2, c4 = (tid & 3) * 4;  // terms as one pass over m)
-        const float2* arow = reinterpret_cast<const float2*>(Amat + (32 + r) * kAs + 16);
-        const float* xb = X + 16 * kXs + c4;
-        float4 acc = *reinterpret_cast<const float4*>(Z + r * 32 + c4);
-#pragma unroll
-        for (int m2 = 0; m2 < 8; ++m2) {
-          const float2 am = arow[m2];
-          fma4s(acc, am.x, *reinterpret_cast<const float4*>(xb + 2 * m2 * kXs));
-          fma4s(acc, am.y, *reinterpret_cast<const float4*>(xb + (2 * m2 + 1) * kXs));
-        }
-        *reinterpret_cast<float4*>(Z + r * 32 + c4) = acc;
-      }
-      __syncthreads();
-      {  // C2: X_10 = -X_11 Z
-        const int r = tid >> 3, c4 = (tid & 7) * 4;
-        const float4* xrow = reinterpret_cast<const float4*>(X + (32 + r) * kXs + 32);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-        for (int m4 = 0; m4 < 8; ++m4) {
-          const float4 xm = xrow[m4];
-          const float* zb = Z + 4 * m4 * 32 + c4;
-          fma4s(acc, xm.x, *reinterpret_cast<const float4*>(zb));
-          fma4s(acc, xm.y, *reinterpret_cast<const float4*>(zb + 32));
-          fma4s(acc, xm.z, *reinterpret_cast<const float4*>(zb + 64));
-          fma4s(acc, xm.w, *reinterpret_cast<const float4*>(zb + 96));
-        }
-        *reinterpret_cast<float4*>(X + (32 + r) * kXs + c4) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-      }
-      __syncthreads();  // X is complete
 
       // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
       //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
-      //      decay rows for the U~ product (V stays exact in bf16) ----
-      for (int e = tid; e < kC * 8; e += kPrepThreads) {
+      //      decay rows for the U~ product (V stays exact in bf16).  Unit = (row
+      //      tr, 8 columns c8) ----
+      auto t_unit = [&](int e) {
         const int tr = e >> 3, c8 = e & 7;
         uint32_t w[4], th[4], tl[4];
 #pragma unroll
@@ -951,7 +932,85 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
             make_uint4(th[0], th[1], th[2], th[3]);
         *reinterpret_cast<uint4*>(sm + kPrepTlo + sw128_chunk(tr, c8, kC)) =
             make_uint4(tl[0], tl[1], tl[2], tl[3]);
+      };
+      bool solved = true;
+      if (warp == 0) {
+        // 6b. A = X_11 (X rows 32..63, columns 32..63) to TMEM lane = row - 32
+        {
+          const float4* xr = reinterpret_cast<const float4*>(X + (32 + lane) * kXs + 32);
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 x4 = xr[q4];
+            split2v(make_float2(x4.x, x4.y), hi[2 * q4], lo[2 * q4]);
+            split2v(make_float2(x4.z, x4.w), hi[2 * q4 + 1], lo[2 * q4 + 1]);
+          }
+          tmem_st16(taddr(tmem, 0, kTdX11), hi);
+          tmem_st16(taddr(tmem, 0, kTdX11 + 16), lo);
+        }
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        // D = X_11 A_10 (K = 32: two steps of 16 = 8 TMEM columns, 32 bytes of
+        // each B row)
+        auto inv_mma = [&](uint32_t a_col, uint32_t d_col, uint32_t bh, uint32_t bl) {
+          fence_after_sync();
+          const uint64_t dh = desc_k_sw128(smem_u32(sm + bh), 0);
+          const uint64_t dl = desc_k_sw128(smem_u32(sm + bl), 0);
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            const uint32_t ah = tmem + a_col + 8 * ks, al = ah + 16;
+            mma_ts(tmem + d_col, ah, dh + 2 * ks, kIdInv, ks ? 1u : 0u);
+            mma_ts(tmem + d_col, ah, dl + 2 * ks, kIdInv, 1u);
+            mma_ts(tmem + d_col, al, dh + 2 * ks, kIdInv, 1u);
+          }
+          mma_commit(&bar_mma);
+        };
+        if (lane == 0) inv_mma(kTdX11, kTdY, kPrepA10h, kPrepA10l);
+        // the B operand -X_00^T while the first product runs: unit (column c =
+        // lane, 8 rows m8)
+#pragma unroll
+        for (int m8 = 0; m8 < 4; ++m8) b_tile(X, kXs, -1.f, kPrepX00h, kPrepX00l, lane, m8);
+        fence_proxy_async();
+        solved = mbar_wait(&bar_mma, mma_phase, t.spins);
+        if (solved) {
+          mma_phase ^= 1;
+          fence_after_sync();
+          uint32_t y[32], hi[16], lo[16];
+          tmem_ld32(taddr(tmem, 0, kTdY), y);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            split2v(make_float2(__uint_as_float(y[2 * u]), __uint_as_float(y[2 * u + 1])),
+                    hi[u], lo[u]);
+          tmem_st16(taddr(tmem, 0, kTdYs), hi);
+          tmem_st16(taddr(tmem, 0, kTdYs + 16), lo);
+          tmem_wait_st();
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) inv_mma(kTdYs, kTdX10, kPrepX00h, kPrepX00l);
+          solved = mbar_wait(&bar_mma, mma_phase, t.spins);
+          if (solved) {
+            mma_phase ^= 1;
+            fence_after_sync();
+            tmem_ld32(taddr(tmem, 0, kTdX10), y);
+            tmem_wait_ld();
+            float4* xo = reinterpret_cast<float4*>(X + (32 + lane) * kXs);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              xo[q4] = make_float4(__uint_as_float(y[4 * q4]), __uint_as_float(y[4 * q4 + 1]),
+                                   __uint_as_float(y[4 * q4 + 2]), __uint_as_float(y[4 * q4 + 3]));
+          }
+        }
+        fence_before_sync();
+      } else {
+        // T rows 0..31 need only X_00
+        for (int e = tid - 32; e < 32 * 8; e += kPrepThreads - 32) t_unit(e);
       }
+      ok = __syncthreads_and(solved);  // X is complete
+      if (!ok) goto fail;
+      fence_after_sync();
+      t_unit(32 * 8 + tid);  // T rows 32..63
       // the v rows have landed once bar_v completes; the barrier that checks it
       // is the one before the products (after the convolution's first barrier
       // when the convolution is on)
