@@ -438,7 +438,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     tok0_ = s0_ + (gid_ - t.chunk_base[n_]) * kC;
     len_ = min(kC, s1_ - tok0_);
   };
+  // per-thread values of the item whose copies are in flight: beta of row tid
+  // and, with decay logits, the scale and channel tid's bias (global loads whose
+  // latency the copies' wait covers)
+  // (beta as its raw bf16 bits, widened only when used)
+  uint32_t pre_beta = 0u;
+  float pre_scale = 1.f, pre_bias = 0.f;
   auto issue_inputs = [&](int h, int tok0, int len, int n, int s0) {
+    if (tid < kD) {
+      pre_beta = 0u;
+      if (tid < len) pre_beta = reinterpret_cast<const uint16_t*>(beta)[(size_t)(tok0 + tid) * H + h];
+      if constexpr (kLogit) {
+        if (a.decay_scale) pre_scale = a.decay_scale[h];
+        if (a.decay_bias) pre_bias = a.decay_bias[(size_t)h * kD + tid];
+      }
+    }
     // the raw q, k, v rows of the 3 tokens before the chunk (short convolution):
     // from the token arrays inside the sequence, else from the caller's window
     // (zeros without one)
@@ -550,15 +564,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
     // ---- 2. running log2-decay per channel (warps 0-3, the channel's 64 rows in
     //      registers); L2 norms of the q, k rows (warps 4-7, one row per thread) ----
     if (tid < kD) {  // thread tid scans channel tid of the rows
-      // beta of row tid: loaded here, stored after the scan, so that the scan hides
-      // its latency
-      float bt = 0.f;
-      if (tid < len) bt = __bfloat162float(beta[(size_t)(tok0 + tid) * H + h]);
-      float dA = 1.f, db = 0.f;  // decay from logits: scale and this channel's bias
-      if constexpr (kLogit) {
-        if (a.decay_scale) dA = a.decay_scale[h];
-        if (a.decay_bias) db = a.decay_bias[(size_t)h * kD + tid];
-      }
+      // beta of row tid (stored after the scan) and the decay logits' scale and
+      // bias of channel tid: loaded when the item's copies were issued
+      const float bt = __uint_as_float(pre_beta << 16), dA = pre_scale, db = pre_bias;
       float x[kC];
 #pragma unroll
       for (int r = 0; r < kC; ++r) x[r] = G[gidx(r, tid)];
@@ -831,7 +839,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       //      (fp32, named barrier), and warp 0 forms the lower 32-block
       //      X_10 = -X_11 A_10 X_00 = (X_11 A_10) (-X_00) by two bf16 hi/lo
       //      products on the tensor cores (as the Gram), while the other warps
-      //      write T's first 32 rows ----
+      //      write the parts of T that need no X_10 ----
       float* X = reinterpret_cast<float*>(sm + kPrepInv);
       float* Y = reinterpret_cast<float*>(sm + kPrepY);
       // K-major bf16 hi/lo tile of the B operand tile[c][m] = sgn * src[m][c]
@@ -912,16 +920,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 
       // ---- 7. T = X Diag(beta): [T; T] (K-major [t][j] fp16, rows 64..127 repeat
       //      rows 0..63) over A for the W product; T as a bf16 hi/lo pair over the
-      //      decay rows for the U~ product (V stays exact in bf16).  Unit = (row
-      //      tr, 8 columns c8) ----
-      auto t_unit = [&](int e) {
-        const int tr = e >> 3, c8 = e & 7;
+      //      decay rows for the U~ product (V stays exact in bf16).  Written by
+      //      row and 8-column group: the block of X_10 by warp 0 from its
+      //      registers, the rest by the other warps while warp 0's products run ----
+      // T columns 8 c8 .. 8 c8 + 7 of row tr from the 8 values x of X
+      auto t_store = [&](int tr, int c8, const float (&x)[8]) {
         uint32_t w[4], th[4], tl[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int j0 = 8 * c8 + 2 * u;
-          const float2 x2 = *reinterpret_cast<const float2*>(X + tr * kXs + j0);
-          const float2 t2 = make_float2(x2.x * s_beta[j0], x2.y * s_beta[j0 + 1]);
+          const float2 t2 = make_float2(x[2 * u] * s_beta[j0], x[2 * u + 1] * s_beta[j0 + 1]);
           w[u] = pack_half2(t2.x, t2.y);
           split2v(t2, th[u], tl[u]);
         }
@@ -932,6 +940,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
             make_uint4(th[0], th[1], th[2], th[3]);
         *reinterpret_cast<uint4*>(sm + kPrepTlo + sw128_chunk(tr, c8, kC)) =
             make_uint4(tl[0], tl[1], tl[2], tl[3]);
+      };
+      // unit e: the rows of T that need no X_10 (rows 0..31, then the columns
+      // 32..63 of rows 32..63), 8 columns each
+      auto t_unit = [&](int e) {
+        const int tr = e < 256 ? e >> 3 : 32 + ((e - 256) >> 2);
+        const int c8 = e < 256 ? e & 7 : 4 + (e & 3);
+        const float4 a4 = *reinterpret_cast<const float4*>(X + tr * kXs + 8 * c8);
+        const float4 b4 = *reinterpret_cast<const float4*>(X + tr * kXs + 8 * c8 + 4);
+        const float x[8] = {a4.x, a4.y, a4.z, a4.w, b4.x, b4.y, b4.z, b4.w};
+        t_store(tr, c8, x);
       };
       bool solved = true;
       if (warp == 0) {
@@ -993,24 +1011,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
           if (solved) {
             mma_phase ^= 1;
             fence_after_sync();
+            // T rows 32..63, columns 0..31 straight from X_10 (lane = row - 32)
             tmem_ld32(taddr(tmem, 0, kTdX10), y);
             tmem_wait_ld();
-            float4* xo = reinterpret_cast<float4*>(X + (32 + lane) * kXs);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              xo[q4] = make_float4(__uint_as_float(y[4 * q4]), __uint_as_float(y[4 * q4 + 1]),
-                                   __uint_as_float(y[4 * q4 + 2]), __uint_as_float(y[4 * q4 + 3]));
+            for (int c8 = 0; c8 < 4; ++c8) {
+              float x[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(y[8 * c8 + j]);
+              t_store(32 + lane, c8, x);
+            }
           }
         }
         fence_before_sync();
       } else {
-        // T rows 0..31 need only X_00
-        for (int e = tid - 32; e < 32 * 8; e += kPrepThreads - 32) t_unit(e);
+        for (int e = tid - 32; e < 32 * 8 + 32 * 4; e += kPrepThreads - 32) t_unit(e);
       }
-      ok = __syncthreads_and(solved);  // X is complete
+      ok = __syncthreads_and(solved);  // T is complete
       if (!ok) goto fail;
-      fence_after_sync();
-      t_unit(32 * 8 + tid);  // T rows 32..63
       // the v rows have landed once bar_v completes; the barrier that checks it
       // is the one before the products (after the convolution's first barrier
       // when the convolution is on)
