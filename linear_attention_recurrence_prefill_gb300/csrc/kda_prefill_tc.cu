@@ -384,9 +384,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PrefillArgs& a = t.a;
 
-  // ---- work items: (chunk, head) pairs, item w = h * total + gid; a CTA takes
-  //      items blockIdx.x, + gridDim.x, ... and streams the next item's inputs
-  //      into its buffers while it writes out the current one ----
+  // ---- work items: (chunk, head) pairs in the order of `decode` below; a CTA
+  //      takes items blockIdx.x, + gridDim.x, ... and streams the next item's
+  //      inputs into its buffers while it writes out the current one ----
   // the chain may start its CTAs (set-up only) as SMs free up at this grid's end
   grid_launch_dependents();
   // sequences of one length L (no cu_seqlens) have ceil(L / C) chunks each: the
@@ -422,16 +422,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
   fence_after_sync();
   const uint32_t tmem = tmem_base;
 
+  // Items run chunk position by chunk position, the heads (and sequences) of one
+  // position side by side, and the last position first: the CTAs in flight read
+  // neighbouring token rows, and the blocks written last (still in L2 when the
+  // chain starts) are the ones the chain reads first.
   auto decode = [&](int wi, int& gid_, int& h_, int& tok0_, int& len_, int& n_, int& s0_) {
-    h_ = wi / total;
-    gid_ = wi - h_ * total;
-    if (!a.cu_seqlens) {
-      n_ = gid_ / cps_eq;
+    const int wr = items - 1 - wi;
+    if (!a.cu_seqlens) {  // wr = (position p, sequence n, head h)
+      const int nh = a.N * a.H;
+      const int p = wr / nh, rem = wr - p * nh;
+      n_ = rem / a.H;
+      h_ = rem - n_ * a.H;
+      gid_ = n_ * cps_eq + p;
       s0_ = n_ * L_eq;
-      tok0_ = s0_ + (gid_ - n_ * cps_eq) * kC;
+      tok0_ = s0_ + p * kC;
       len_ = min(kC, (n_ + 1) * L_eq - tok0_);
       return;
     }
+    gid_ = wr / a.H;  // wr = (chunk, head)
+    h_ = wr - gid_ * a.H;
     n_ = find_seq(t.chunk_base, a.N, gid_);
     int s1_;
     seq_range(a.cu_seqlens, a.N, a.T_total, n_, s0_, s1_);
