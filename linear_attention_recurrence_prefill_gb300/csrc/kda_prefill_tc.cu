@@ -84,7 +84,6 @@ __constant__ uint32_t kWsPartLen[kWsParts] = {16384, 32768, 16384, 8192, 512};
 
 constexpr uint32_t kIdGram = idesc_f16(128, 96, true);      // Gram: M128 N96 bf16
 constexpr uint32_t kIdF16N64 = idesc_f16(128, 64, false);   // fp16, N = 64
-constexpr uint32_t kIdF16N128 = idesc_f16(128, 128, false); // fp16, N = 128
 constexpr uint32_t kIdKh = idesc_f16(128, 128, false, false, true);  // fp16, N = 128, B MN-major
 
 struct TcArgs {
@@ -1192,10 +1191,10 @@ done:
 // 512 threads.  Warps 0-7 carry the state (conversions split by column half;
 // thread 0 also issues the MMAs); warps 8-15 run the epilogue from a
 // double-buffered O^T, overlapping the next chunk, and their first thread
-// issues the bulk load of chunk i + 2 as soon as chunk i's MMAs are done.  Warp w touches TMEM lanes 32*(w%4) .. +31 (lane = d_v index).  Per
-// chunk i:
+// issues the bulk load of chunk i + 2 as soon as chunk i's MMAs are done.  Warp
+// w touches TMEM lanes 32*(w%4) .. +31 (lane = d_v index).  Per chunk i:
 //   -S^T -> fp16 operand, S^T <- S^T Diag(G_C)   (state warps)
-//   [D | O^T] = (-S^T) [W ; -Q~]^T              (8 MMAs, N = 128)
+//   D = (-S^T) W^T, then O^T = (-S^T)(-Q~)^T     (8 + 8 MMAs, N = 64; D first)
 //   U^T = U~^T + D -> fp16 operand               (state warps, U~^T from the block)
 //   S^T += U^T K^ (the critical path), O^T += U^T P^T
 //   y rows from O^T                              (epilogue warps)
@@ -1347,18 +1346,25 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
       bool woe = true;
       if (tid == 0) {
         fence_after_sync();
-        // the product overwrites [U | O] buffer i & 1: O^T(i - 2) must be copied out
-        if (i >= 2) woe = mbar_wait(&bar_oe[i & 1], ((i - 2) >> 1) & 1, t.spins);
+        // U^T - U~^T = (-S^T) W^T into columns 0..63 of [U | O] buffer i & 1, the
+        // state chain's product, committed on its own; then O^T = (-S^T)(-Q~)^T
+        // into columns 64..127, once the epilogue has copied O^T(i - 2) out of
+        // them (bar_s below covers it).  B = rows 0..63 (W) or 64..127 (-Q~: +8 KB,
+        // +512 in the descriptor's address field) of the tile; K-step: +2 (32
+        // bytes); K-block of 64: +1024 (16 KB)
         const uint64_t dWQ = desc_k_sw128(smem_u32(buf) + kWsWQ, 0);
-        // [U^T - U~^T | O^T] = (-S^T) [W ; -Q~]^T.  K-step: +2 in the descriptor's
-        // address field (32 bytes); K-block of 64: +1024 (16 KB)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N64,
+                 ks > 0);
+        mma_commit(&bar_u);
+        if (i >= 2) woe = mbar_wait(&bar_oe[i & 1], ((i - 2) >> 1) & 1, t.spins);
         if (woe) {
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tUO, tmem + kTAS + 8 * ks, dWQ + 1024 * (ks >> 2) + 2 * (ks & 3), kIdF16N128,
-                   ks > 0);
+            mma_ts(tUO + 64, tmem + kTAS + 8 * ks, dWQ + 512 + 1024 * (ks >> 2) + 2 * (ks & 3),
+                   kIdF16N64, ks > 0);
         }
-        mma_commit(&bar_u);
       }
       // S^T <- S^T Diag(G_C) while the product runs (only S^T += U^T K^ below
       // reads it; the wait before that barrier covers these stores)
