@@ -204,18 +204,22 @@ constexpr uint32_t kPrepStU = kPrepX, kPrepStW = kPrepX + 16384;
 constexpr uint32_t kPrepA10h = kPrepG + 16384, kPrepA10l = kPrepA10h + 4096;
 constexpr uint32_t kPrepX00h = kPrepA10h + 8192, kPrepX00l = kPrepA10h + 12288;
 // TMEM: the Gram's D = [D_0 | D_1] (32 + 64 columns) and A (hi, lo for each
-// channel half: 4 x 32); then U~^T (64 columns) and W (128)
+// channel half: 4 x 32); then U~^T as its T_hi and T_lo parts (2 x 64 columns)
+// and W (128)
 constexpr uint32_t kPrepTmemCols = 256, kTdD0 = 0, kTdD1 = 32, kTdA = 96;
-constexpr uint32_t kTdU = 0, kTdW = 64;
+constexpr uint32_t kTdU = 0, kTdW = 128;
 // the inverse (between the two): lanes 0..31 carry rows 32..63; A = X_11 as
-// bf16 hi/lo (16 + 16 columns), D = X_11 A_10, A = that product as hi/lo, and
-// D = X_10
-constexpr uint32_t kTdX11 = 128, kTdY = 160, kTdYs = 192, kTdX10 = 224;
-static_assert(kTdX10 + 32 <= kPrepTmemCols, "the inverse's operands fit the TMEM allocation");
-constexpr uint32_t kIdInv = idesc_f16(128, 32, true);  // bf16, N = 32
+// bf16 hi/lo (16 + 16 columns), D = X_11 A_10 (64 columns: hi.hi + lo.hi, then
+// hi.lo), A = that product as hi/lo, and D = X_10 (64 columns likewise, over
+// X_11's and the first product's, both read by then)
+constexpr uint32_t kTdX11 = 128, kTdY = 160, kTdYs = 224, kTdX10 = 128;
+static_assert(kTdY + 64 <= kTdYs && kTdYs + 32 <= kPrepTmemCols,
+              "the inverse's operands fit the TMEM allocation");
+constexpr uint32_t kIdInv32 = idesc_f16(128, 32, true);  // bf16, N = 32
+constexpr uint32_t kIdInv64 = idesc_f16(128, 64, true);  // bf16, N = 64
 static_assert(kTdA + 128 <= kPrepTmemCols, "Gram accumulators and A fit the TMEM allocation");
-static_assert(kTdW + 128 <= kPrepTmemCols, "W fits the TMEM allocation");
-constexpr uint32_t kIdUt = idesc_f16(128, 64, true, true, false);   // bf16, A MN-major, N = 64
+static_assert(kTdU + 128 <= kTdW && kTdW + 128 <= kPrepTmemCols, "U~^T and W fit the TMEM allocation");
+constexpr uint32_t kIdUt = idesc_f16(128, 128, true, true, false);  // bf16, A MN-major, N = 128
 constexpr uint32_t kIdW = idesc_f16(128, 128, false, false, true);  // B MN-major, N = 128
 constexpr uint32_t kPrepSmall = kPrepX + 40960;  // inv_q, inv_k, beta [64] fp32
 // short convolution: the raw q, k, v rows of the 3 tokens before the chunk,
@@ -978,21 +982,24 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         fence_before_sync();
         __syncwarp();
         // D = X_11 A_10 (K = 32: two steps of 16 = 8 TMEM columns, 32 bytes of
-        // each B row)
-        auto inv_mma = [&](uint32_t a_col, uint32_t d_col, uint32_t bh, uint32_t bl) {
+        // each B row).  The B tile's hi and lo halves are one 64-row tile, so
+        // A_hi [B_hi; B_lo]^T is one N = 64 product (columns 0..31: hi.hi, 32..63:
+        // hi.lo) and A_lo B_hi^T accumulates into columns 0..31: 4 MMAs, each
+        // costing the issuing thread about as much as one of N = 32
+        auto inv_mma = [&](uint32_t a_col, uint32_t d_col, uint32_t bh) {
           fence_after_sync();
           const uint64_t dh = desc_k_sw128(smem_u32(sm + bh), 0);
-          const uint64_t dl = desc_k_sw128(smem_u32(sm + bl), 0);
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
             const uint32_t ah = tmem + a_col + 8 * ks, al = ah + 16;
-            mma_ts(tmem + d_col, ah, dh + 2 * ks, kIdInv, ks ? 1u : 0u);
-            mma_ts(tmem + d_col, ah, dl + 2 * ks, kIdInv, 1u);
-            mma_ts(tmem + d_col, al, dh + 2 * ks, kIdInv, 1u);
+            mma_ts(tmem + d_col, ah, dh + 2 * ks, kIdInv64, ks ? 1u : 0u);
+            mma_ts(tmem + d_col, al, dh + 2 * ks, kIdInv32, 1u);
           }
           mma_commit(&bar_mma);
         };
-        if (lane == 0) inv_mma(kTdX11, kTdY, kPrepA10h, kPrepA10l);
+        static_assert(kPrepA10l == kPrepA10h + 32 * 128 && kPrepX00l == kPrepX00h + 32 * 128,
+                      "each B operand's lo tile follows its hi tile as rows 32..63");
+        if (lane == 0) inv_mma(kTdX11, kTdY, kPrepA10h);
         // the B operand -X_00^T while the first product runs: unit (column c =
         // lane, 8 rows m8)
 #pragma unroll
@@ -1002,31 +1009,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         if (solved) {
           mma_phase ^= 1;
           fence_after_sync();
-          uint32_t y[32], hi[16], lo[16];
+          uint32_t y[32], y2[32], hi[16], lo[16];
           tmem_ld32(taddr(tmem, 0, kTdY), y);
+          tmem_ld32(taddr(tmem, 0, kTdY + 32), y2);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 16; ++u)
-            split2v(make_float2(__uint_as_float(y[2 * u]), __uint_as_float(y[2 * u + 1])),
+            split2v(make_float2(__uint_as_float(y[2 * u]) + __uint_as_float(y2[2 * u]),
+                                __uint_as_float(y[2 * u + 1]) + __uint_as_float(y2[2 * u + 1])),
                     hi[u], lo[u]);
           tmem_st16(taddr(tmem, 0, kTdYs), hi);
           tmem_st16(taddr(tmem, 0, kTdYs + 16), lo);
           tmem_wait_st();
           fence_before_sync();
           __syncwarp();
-          if (lane == 0) inv_mma(kTdYs, kTdX10, kPrepX00h, kPrepX00l);
+          if (lane == 0) inv_mma(kTdYs, kTdX10, kPrepX00h);
           solved = mbar_wait(&bar_mma, mma_phase, t.spins);
           if (solved) {
             mma_phase ^= 1;
             fence_after_sync();
             // T rows 32..63, columns 0..31 straight from X_10 (lane = row - 32)
             tmem_ld32(taddr(tmem, 0, kTdX10), y);
+            tmem_ld32(taddr(tmem, 0, kTdX10 + 32), y2);
             tmem_wait_ld();
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
               float x[8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) x[j] = __uint_as_float(y[8 * c8 + j]);
+              for (int j = 0; j < 8; ++j)
+                x[j] = __uint_as_float(y[8 * c8 + j]) + __uint_as_float(y2[8 * c8 + j]);
               t_store(32 + lane, c8, x);
             }
           }
@@ -1083,12 +1094,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
 
       // ---- 8. U~^T = V^T (T_hi + T_lo)^T (A = V MN-major bf16) and W = [T; T] K~
       //      (B = K~ MN-major fp16) on the tensor cores, then both straight to the
-      //      workspace ----
+      //      workspace.  The T_hi and T_lo tiles are one 128-row tile, so U~^T is
+      //      one N = 128 product per K-step with its hi and lo parts side by side
+      //      (summed on the way out): 8 MMAs ----
+      static_assert(kPrepTlo == kPrepThi + kC * 128, "T_lo follows T_hi as rows 64..127");
       if (tid == 0) {
         fence_after_sync();
         const uint32_t sT = smem_u32(sm + kPrepTT), sV = smem_u32(sm + kPrepV);
         const uint32_t sKt = smem_u32(sm + kPrepKt);
-        const uint32_t sTh = smem_u32(sm + kPrepThi), sTl = smem_u32(sm + kPrepTlo);
+        const uint32_t sTh = smem_u32(sm + kPrepThi);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTh, 32 * ks),
@@ -1096,10 +1110,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
           mma_ss(tmem + kTdW, desc_k_sw128(sT, 32 * ks), desc_mn_sw128(sKt, ks, kC * 128),
                  kIdW, ks > 0);
         }
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tmem + kTdU, desc_mn_sw128(sV, ks, kC * 128), desc_k_sw128(sTl, 32 * ks),
-                 kIdUt, 1u);
         mma_commit(&bar_mma);
       }
       ok = __syncthreads_and(mbar_wait(&bar_mma, mma_phase, t.spins));
@@ -1126,6 +1136,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         const int lrow = quarter * 32 + lane, slab = 2 * chalf + (quarter >> 1);
         uint32_t x[32], y[32];
         tmem_ld32(taddr(tmem, quarter * 32, kTdU + 32 * chalf), x);
+        tmem_ld32(taddr(tmem, quarter * 32, kTdU + 64 + 32 * chalf), y);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)  // the T_hi and T_lo parts of U~^T
+          x[j] = __float_as_uint(__uint_as_float(x[j]) + __uint_as_float(y[j]));
         tmem_ld32(taddr(tmem, quarter * 32, kTdW + 32 * slab), y);
         tmem_wait_ld();
 #pragma unroll
