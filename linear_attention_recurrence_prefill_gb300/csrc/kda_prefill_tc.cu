@@ -581,21 +581,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       const float bt = __uint_as_float(pre_beta << 16), dA = pre_scale, db = pre_bias;
       float x[kC];
 #pragma unroll
-      for (int r = 0; r < kC; ++r) x[r] = G[gidx(r, tid)];
-      float run = 0.f;
-      if constexpr (kLogit) {  // log alpha = g_min sigmoid(A (z + b)); rows past
-#pragma unroll                   // the sequence end stay at 0 (identity steps)
-        for (int r = 0; r < kC; ++r) {
-          const float la = r < len ? a.g_min * sigmoid_fast(dA * (x[r] + db)) : 0.f;
-          run += fminf(fmaxf(la, a.g_min), 0.f) * kLog2e;
-          x[r] = run;
-        }
-      } else {  // rows past the sequence end: log alpha 0
+      for (int r = 0; r < kC; ++r) {
+        x[r] = G[gidx(r, tid)];
+        if constexpr (kLogit) x[r] = a.g_min * sigmoid_fast(dA * (x[r] + db));  // g_min sigmoid(A (z + b))
+        x[r] = fminf(fmaxf(x[r], a.g_min), 0.f);
+      }
+      if (len < kC) {  // rows past the sequence end: log alpha 0 (identity steps)
 #pragma unroll
-        for (int r = 0; r < kC; ++r) {
-          run += (r < len ? fminf(fmaxf(x[r], a.g_min), 0.f) : 0.f) * kLog2e;
-          x[r] = run;
-        }
+        for (int r = 0; r < kC; ++r)
+          if (r >= len) x[r] = 0.f;
+      }
+      float run = 0.f;
+#pragma unroll
+      for (int r = 0; r < kC; ++r) {
+        run += x[r] * kLog2e;
+        x[r] = run;
       }
 #pragma unroll
       for (int r = 0; r < kC; ++r) G[gidx(r, tid)] = x[r];
@@ -606,7 +606,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       // warp's loads hit every bank
       const int rr = tid - kD, r = rr & (kC - 1);
       const uint8_t* src = sm + (rr < kC ? kPrepQ : kPrepK) + r * 128;
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 s2[4] = {};  // packed f32x2 sums of squares (even, odd channel of a pair)
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int p = (i + rr) & 15;  // physical chunk: half p / 8, position p % 8
@@ -614,12 +614,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
         const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float lo = __uint_as_float(wv[u] << 16), hi = __uint_as_float(wv[u] & 0xFFFF0000u);
-          s4[u] = fmaf(lo, lo, s4[u]);
-          s4[u] = fmaf(hi, hi, s4[u]);
+          const float2 v2 = make_float2(__uint_as_float(wv[u] << 16), __uint_as_float(wv[u] & 0xFFFF0000u));
+          s2[u] = fma2(v2, v2, s2[u]);
         }
       }
-      const float sl = (s4[0] + s4[1]) + (s4[2] + s4[3]) + a.eps_l2;
+      const float sl = ((s2[0].x + s2[0].y) + (s2[1].x + s2[1].y)) +
+                       ((s2[2].x + s2[2].y) + (s2[3].x + s2[3].y)) + a.eps_l2;
       const float inv = a.l2norm_qk ? (sl > 0.f ? rsqrtf(sl) : 0.f) : 1.f;
       if (rr < kC) s_invq[r] = inv * a.q_scale;
       else s_invk[r] = inv;
