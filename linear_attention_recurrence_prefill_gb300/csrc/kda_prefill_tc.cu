@@ -109,10 +109,16 @@ __device__ __forceinline__ uint8_t* ws_block(const TcArgs& t, int chunk_id, int 
 }
 
 // ============================================================ chunk bases
-// base[n] = sum_{m < n} ceil(len_m / C); also checks cu_seqlens.
+// base[n] = sum_{m < n} ceil(len_m / C); also checks cu_seqlens.  Behind the
+// bases (at base + N + 1) it writes the order in which the chain grid takes the
+// sequences: by descending chunk count (ties by index), so that the longest
+// chains start first and the grid's last wave holds short ones; for more than
+// kOrderMax sequences the order stays the index order.
+constexpr int kOrderMax = 2048;
 __global__ void __launch_bounds__(1024) chunk_base_kernel(TcArgs t) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
+  __shared__ int s_cnt[kOrderMax];  // chunks per sequence (N <= kOrderMax)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     carry = 0;
@@ -151,9 +157,20 @@ __global__ void __launch_bounds__(1024) chunk_base_kernel(TcArgs t) {
     __syncthreads();
     const int before = carry + (warp ? warp_tot[warp - 1] : 0);
     if (n < t.a.N) t.chunk_base[n + 1] = before + incl;
+    if (n < t.a.N && t.a.N <= kOrderMax) s_cnt[n] = cnt;
     __syncthreads();
     if (tid == 0) carry += warp_tot[31];
     __syncthreads();
+  }
+  int* order = t.chunk_base + t.a.N + 1;
+  for (int n = tid; n < t.a.N; n += 1024) {
+    int rank = n;
+    if (t.a.N <= kOrderMax) {  // position among the sequences, longest first
+      const int c = s_cnt[n];
+      rank = 0;
+      for (int m = 0; m < t.a.N; ++m) rank += (s_cnt[m] > c || (s_cnt[m] == c && m < n)) ? 1 : 0;
+    }
+    order[rank] = n;
   }
 }
 
@@ -1251,7 +1268,10 @@ __global__ void __launch_bounds__(kChThreads, 1) chain_kernel(TcArgs t) {
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;  // TMEM lane of this thread = d_v index
   const PrefillArgs& a = t.a;
-  const int h = blockIdx.x % a.H, n = blockIdx.x / a.H;
+  // packed sequences: CTA b takes head b % H of the sequence at position b / H
+  // of the chunk-base kernel's order (longest first)
+  const int h = blockIdx.x % a.H;
+  const int n = a.cu_seqlens ? t.chunk_base[a.N + 1 + (int)blockIdx.x / a.H] : (int)blockIdx.x / a.H;
   const size_t H = (size_t)a.H;
   int s0, s1;
   seq_range(a.cu_seqlens, a.N, a.T_total, n, s0, s1);
@@ -1627,7 +1647,8 @@ bool encode_rows(CUtensorMap* m, const void* base, int T, int H, bool fp32) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t header_bytes(int N) { return ((size_t)(N + 1) * 4 + 1023) & ~(size_t)1023; }
+// workspace header: the chunk bases [N + 1] and the chain's sequence order [N]
+size_t header_bytes(int N) { return ((size_t)(2 * N + 1) * 4 + 1023) & ~(size_t)1023; }
 int chunks_upper(int T_total, int N) { return T_total / kC + N; }
 
 }  // namespace

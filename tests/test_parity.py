@@ -124,6 +124,31 @@ def test_many_short_sequences(impl):
     assert empty and torch.equal(S_T[empty], inp.S0[empty])
 
 
+def test_chain_order_longest_first():
+    """With packed sequences the chunk-base kernel leaves, behind the N + 1 chunk
+    bases at the head of the workspace, the order in which the chain grid takes
+    the sequences: a permutation by descending chunk count, ties by index (the
+    results themselves do not depend on it: each chain CTA is one sequence and
+    head)."""
+    dev = _cuda()
+    lens = [70, 0, 640, 33, 64, 65, 129, 640, 1, 200]
+    inp = inputs.varlen(dev, H=2, lengths=lens)
+    need = kda.kda_prefill_workspace_size(inp.T, len(lens), inp.H, 128, 128)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    o, S_T = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, None,
+                             inp.cu_seqlens, len(lens), gate=inp.gate, impl="tc", workspace=ws)
+    torch.cuda.synchronize()
+    N = len(lens)
+    head = ws[: (2 * N + 1) * 4].cpu().view(torch.int32).tolist()
+    chunks = [(L + 63) // 64 for L in lens]
+    base = [0]
+    for c in chunks:
+        base.append(base[-1] + c)
+    assert head[: N + 1] == base
+    assert head[N + 1:] == sorted(range(N), key=lambda n: (-chunks[n], n))
+    _check(inp, "tc", TOL_BF16)
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_varlen_equals_separate_calls(impl):
     """Packed sequences give exactly what separate calls on each one give: every
