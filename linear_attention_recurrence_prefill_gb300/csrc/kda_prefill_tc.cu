@@ -20,8 +20,10 @@
 //                          running sum), the decay-rescaled Gram matrices A and P on the
 //                          tensor cores (bf16 hi/lo split, three products, fp32
 //                          accumulation in TMEM), the unit-lower-triangular solve
-//                          T = (I + A)^-1 Diag(beta) in fp32, then W = T K~ and
-//                          U~ = T V on the tensor cores.  Writes one 72.5 KB
+//                          T = (I + A)^-1 Diag(beta) (fp32 diagonal blocks, the
+//                          lower 32-block as two bf16 hi/lo tensor-core
+//                          products), then W = T K~ and U~ = T V on the tensor
+//                          cores.  Writes one 72.5 KB
 //                          block per (chunk, head) to the workspace, already in
 //                          the shared-memory operand layout of kernel 3.
 //   3. chain_kernel        one CTA per (sequence, head), launched early
@@ -46,10 +48,12 @@
 // V, K~ and K^ enter their products as MN-major operands (64-channel blocks of
 // token rows), so every one of them is produced row by row, like the inputs.
 //
-// Precision: the Gram products use a bf16 hi/lo split (hi*hi + hi*lo + lo*hi,
-// ~16 significant bits, bf16 keeps the 2^+-116 range); every other product uses
-// fp16 operands (11 significant bits; all values there are within fp16 range
-// or negligibly small) with fp32 accumulation; the state itself stays fp32.
+// Precision: the Gram products and the inverse's lower block use a bf16 hi/lo
+// split (hi*hi + hi*lo + lo*hi, ~16 significant bits, bf16 keeps the 2^+-116
+// range), U~ = T V takes T as a bf16 hi/lo pair against V exact in bf16, and
+// every other product uses fp16 operands (11 significant bits; all values there
+// are within fp16 range or negligibly small) with fp32 accumulation; the state
+// itself stays fp32.
 #include <cuda.h>
 #include <stdio.h>
 
