@@ -986,7 +986,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const __grid_cons
       };
       bool solved = true;
       if (warp == 0) {
-        // 6b. A = X_11 (X rows 32..63, columns 32..63) to TMEM lane = row - 32
+        // the lower 32-block: A = X_11 (X rows 32..63, columns 32..63) to TMEM lane = row - 32
         {
           const float4* xr = reinterpret_cast<const float4*>(X + (32 + lane) * kXs + 32);
           uint32_t hi[16], lo[16];
