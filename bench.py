@@ -580,17 +580,22 @@ def _calibrated_heads(inp, target_s: float) -> int:
 def cpu_baseline(args):
     """The oracle, as it stands, on the prefill workload (all OpenMP threads):
     every token of the first `heads` heads, `heads` chosen so that the sample
-    is about 10 s of CPU work (all 96 heads when that fits)."""
+    is about 10 s of CPU work (all 96 heads when that fits).  Beside it the
+    per-core figure: head 0 alone, which the oracle's loop over (sequence,
+    head) gives to one thread."""
     from linear_attention_recurrence_prefill_gb300 import inputs
 
     inp = inputs.k3("cpu")
     heads = _calibrated_heads(inp, args.cpu_seconds)
     dt = _oracle_step(inp, heads)
+    dt1 = min(_oracle_step(inp, 1) for _ in range(2))
     return {"value": heads * T / H / dt, "unit": "tokens/s", "cores": cpu_cores(),
             "kind": "oracle",
             "sample": f"k3 workload, all {T} tokens of the first {heads} of {H} heads "
                       f"({heads * T} head-tokens, {dt:.1f} s); tokens/s = head-tokens/s / {H}",
-            "seconds": dt}
+            "seconds": dt,
+            "single_core": {"value": T / dt1, "unit": "head-tokens/s",
+                            "sample": f"head 0, all {T} tokens, one thread ({dt1:.2f} s)"}}
 
 
 def run_reference(args, rank, world):
