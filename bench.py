@@ -230,6 +230,70 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, by ctypes) every ~1 ms from a thread, so that even a
+    millisecond-long timed region is sampled; nvidia-smi cannot sample faster
+    than its loop interval.  Reads only."""
+
+    # NVML clock-event reason bits (nvml.h): the ones a measurement is checked for
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, index: int):
+        import ctypes
+        import threading
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._lib = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self._h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self._h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(self._h, ctypes.c_int(1), ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._lib = lib
+        except (OSError, AttributeError):
+            self._lib = None
+
+    def _run(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._lib.nvmlDeviceGetClockInfo(self._h, ctypes.c_int(1), ctypes.byref(clk)) == 0 \
+                    and self._reasons_fn(self._h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.001)
+
+    def __enter__(self):
+        import threading
+        if self._lib is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        loaded = [c for c, _ in self.samples if c > 0.5 * max(c for c, _ in self.samples)]
+        reasons = sorted({nm for _, r in self.samples for bit, nm in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml, ~1 ms"}
+
+
 # ------------------------------------------------------------------ our arm
 N_UP = 4  # host->device copy streams of the end-to-end leg
 LEGS = ("prefill", "e2e", "decode", "varlen", "extreme")
@@ -266,18 +330,25 @@ def time_prefill(inp, args, stream, dist, *, steps, warmup, max_seqlen=0, clocks
         raise RuntimeError(f"device status word set during the {inp.name} warm-up")
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clk = ClockSampler(torch.cuda.current_device()) if clocks else None
+    nv = NvmlSampler(torch.cuda.current_device()) if clocks else None
     if clk:
         clk.__enter__()
     try:
         barrier(dist)
         torch.cuda.synchronize()
+        if nv:
+            nv.__enter__()
         ev0.record(stream)
         for _ in range(steps):
             call()
         ev1.record(stream)
         torch.cuda.synchronize()
+        if nv:
+            nv.__exit__(None, None, None)
         barrier(dist)
     finally:
+        if nv:
+            nv.__exit__(None, None, None)
         if clk:
             clk.__exit__(None, None, None)
     ms = max_over_ranks(dist, ev0.elapsed_time(ev1) / steps)
@@ -299,7 +370,8 @@ def time_prefill(inp, args, stream, dist, *, steps, warmup, max_seqlen=0, clocks
     # the tensor-core path skips its first kernel (chunk bases) for equal lengths
     launched = launches - (1 if path == "tc" and inp.cu_seqlens is None else 0)
     return dict(ms=ms, path=path, chunk=chunk, launches=launches, launched=launched,
-                kernel_ms=kern, ws_bytes=ws_bytes, clocks=clk.summary() if clk else None)
+                kernel_ms=kern, ws_bytes=ws_bytes,
+                clocks=((nv.summary() if nv else None) or clk.summary()) if clk else None)
 
 
 def prefill_leg(inp, args, stream, dist, peaks, *, steps, warmup, max_seqlen=0):

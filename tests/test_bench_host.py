@@ -100,3 +100,19 @@ def test_measured_traffic_follows_the_code(tmp_path, monkeypatch):
     assert bench.measured_traffic() == {"k": 1234.0}
     src.write_text("__global__ void k() { int a = 0; }\n")   # the kernel changed
     assert bench.measured_traffic() == {}
+
+
+def test_nvml_sampler_summary():
+    """The clock summary from (SM MHz, clock-event reason bits) samples: the
+    median of the loaded samples, and the named reasons that were set."""
+    import bench
+    nv = bench.NvmlSampler.__new__(bench.NvmlSampler)
+    nv.max_mhz = 2070.0
+    nv.samples = []
+    assert nv.summary() is None
+    nv.samples = [(2070.0, 0), (2055.0, 0x4), (2070.0, 0x1), (400.0, 0)]
+    s = nv.summary()
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["samples"] == 4
+    assert s["reasons"] == ["sw_power_cap"]
+    nv.samples = [(1500.0, 0x8 | 0x40)]
+    assert nv.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
