@@ -9,6 +9,8 @@ max-abs <= 2e-2 and rel-L2 <= 5e-3 for bf16 operands, 1e-4 for the fp32 path.
 """
 from __future__ import annotations
 
+import random
+
 import numpy as np
 import pytest
 import torch
@@ -122,6 +124,31 @@ def test_many_short_sequences(impl):
     o, S_T = _check(inp, impl, TOL_BF16, max_seqlen=max(lens))
     empty = [n for n, L in enumerate(lens) if L == 0]
     assert empty and torch.equal(S_T[empty], inp.S0[empty])
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("case", range(16))
+def test_random_shapes(impl, case):
+    """Seeded random shapes against the oracle: head counts that do not divide
+    the SM count, equal-length batches given with and without cu_seqlens, and
+    packed sequences with empty, single-token and ragged members, with and
+    without the gate."""
+    dev = _cuda()
+    rng = random.Random(1000 + case)
+    H = rng.choice([1, 2, 3, 5, 7, 33])
+    if rng.random() < 0.5:
+        N = rng.choice([1, 2, 3])
+        L = rng.choice([1, 17, 63, 64, 65, 127, 200])
+        inp = inputs.k3(dev, H=H, T=N * L, seed=2000 + case)
+        inp.N = N
+        if N > 1 and rng.random() < 0.5:
+            inp.cu_seqlens = torch.arange(0, N + 1, dtype=torch.int32, device=dev) * L
+    else:
+        lens = [rng.choice([0, 1, 5, 63, 64, 65, 130, 300]) for _ in range(rng.choice([2, 4, 9]))]
+        lens[rng.randrange(len(lens))] = max(1, lens[0])
+        inp = inputs.varlen(dev, H=H, lengths=lens, seed=2000 + case)
+    inp.S0 = torch.randn((inp.N, H, 128, 128), device=dev) * 0.02
+    _check(inp, impl, TOL_BF16, gate=rng.random() < 0.5)
 
 
 def test_chain_order_longest_first():
